@@ -1,0 +1,126 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin.
+
+Each mutant is one plausible slip (a wrong constant, sign, index, operand, rounding rule
+or loop bound) applied by text substitution to a temporary copy of oracle/oracle.cpp,
+compiled with the oracle's own flags, and run against a fast battery of the pins in
+test_oracle_golden / test_oracle_exact / test_oracle_plan.  The committed oracle is never
+changed.
+
+Not listed: computing 1/loss_scale in float instead of double-then-float.  The two agree
+for every binary32 loss scale (rounding a quotient of binary32 values first to 53 bits and
+then to 24 is innocuous, as 53 >= 2*24 + 2), so that mutant is equivalent, not missed."""
+import ctypes
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import build as obuild
+import _golden as G
+import test_oracle_exact as TE
+import test_oracle_golden as TG
+import test_oracle_plan as TP
+
+MUTANTS = {
+    "scale_divisor_128": ("m / 127.0f", "m / 128.0f"),
+    "round_half_away": ("std::nearbyint(g / s)", "std::round(g / s)"),
+    "reciprocal_multiply": ("std::nearbyint(g / s)", "std::nearbyint(g * (1.0f / s))"),
+    "clamp_low_127": ("if (y < -128.0f) y = -128.0f;", "if (y < -127.0f) y = -127.0f;"),
+    "absmax_without_abs": ("const float a = std::fabs(g);", "const float a = g;"),
+    "ring_start_at_t": ("acc = d[(t + 1) % W];\n                for (int k = 2; k <= W; ++k) acc = acc + d[(t + k) % W];",
+                        "acc = d[t % W];\n                for (int k = 1; k < W; ++k) acc = acc + d[(t + k) % W];"),
+    "ring_segment_floor": ("const int64_t seg = (len + W - 1) / W;", "const int64_t seg = len / W + 1;"),
+    "ring_reverse": ("acc = acc + d[(t + k) % W];", "acc = acc + d[(t + W + 2 - k) % W];"),
+    "seq_reverse": ("acc = d[0];\n                for (int r = 1; r < W; ++r) acc = acc + d[r];",
+                    "acc = d[W - 1];\n                for (int r = W - 2; r >= 0; --r) acc = acc + d[r];"),
+    "tree_carry_first": ("if (level.size() % 2 == 1) next.push_back(level.back());",
+                         "if (level.size() % 2 == 1) next.insert(next.begin(), level.back());"),
+    "mean_reciprocal": ("out[i] = acc / static_cast<float>(W);", "out[i] = acc * (1.0f / static_cast<float>(W));"),
+    "mean_missing": ("out[i] = acc / static_cast<float>(W);", "out[i] = acc;"),
+    "scales_transposed": ("d[r] = q * scales[static_cast<int64_t>(r) * num_chunks + j];",
+                          "d[r] = q * scales[j * W + r];"),
+    "chunk_divisor_minus_alignment": ("(kChunkSize - kChunkSize % kAlignment)", "(kChunkSize - kAlignment)"),
+    "chunk_count_is_k": ("return (n + c - 1) / c;             // pieces", "return k;             // pieces"),
+    "chunk_len_floor": ("const int64_t c = (n + k - 1) / k;", "const int64_t c = n / k;"),
+    "plan_missing_bucket_base": ("offsets[pos++] = start + j * c;", "offsets[pos++] = j * c;"),
+    "bucket_cap_inclusive": ("open_bytes + bytes > cap_bytes", "open_bytes + bytes >= cap_bytes"),
+    "unscale_divides": ("return x * inv;", "return x / inv;"),
+    "half_exponent_bias": ("e - 25", "e - 24"),
+    "half_subnormal_scale": ("static_cast<double>(f), -24", "static_cast<double>(f), -25"),
+    "zero_scale_not_special": ("if (finite && s != 0.0f) {", "if (finite) {"),
+}
+
+
+def _battery(orc):
+    """Run the fast pins; return the name of the first failing one, or None."""
+    checks = [
+        ("dynamic_chunk_sizes", lambda: TG.test_dynamic_chunk_sizes(orc)),
+        ("unscale_f16", lambda: TG.test_unscale_f16(orc)),
+        ("reduce_orders", lambda: TG.test_reduce_orders(orc)),
+        ("bucket_assignment", lambda: TG.test_bucket_assignment(orc)),
+        ("multi_bucket", lambda: TP.test_plan_multi_bucket_table(orc)),
+        ("mean_div", lambda: TE.test_mean_division_nonpower_of_two(orc)),
+        ("half_decode", lambda: TE.test_half_decode_all_patterns(orc)),
+    ]
+    for name, case in G.keyed_cases("quantize_cases.txt"):
+        checks.append(("quantize:" + name, lambda c=case, n=name: TG.test_quantize_cases(orc, n, c)))
+    for W in (3, 4, 5):
+        for kind in ("mixed", "normal"):
+            checks.append(("exact:%d:%s" % (W, kind), lambda W=W, k=kind: TE.test_quantize_reduce_exact(orc, W, k)))
+    checks.append(("f16_exact", lambda: TE.test_f16_unscale_exact(orc, 3.0)))
+    checks.append(("f16_exact_65536", lambda: TE.test_f16_unscale_exact(orc, 65536.0)))
+    for name, fn in checks:
+        try:
+            fn()
+        except AssertionError:
+            return name
+    return None
+
+
+def _load(path):
+    saved = oracle._lib
+    oracle._lib = None
+    real_build = obuild.build
+    obuild.build = lambda force=False: path
+    try:
+        oracle.lib()
+        return oracle._lib
+    finally:
+        obuild.build = real_build
+        oracle._lib = saved
+
+
+class _Swap:
+    def __init__(self, lib):
+        self.lib = lib
+
+    def __enter__(self):
+        self.saved = oracle._lib
+        oracle._lib = self.lib
+        return oracle
+
+    def __exit__(self, *a):
+        oracle._lib = self.saved
+
+
+def test_unmutated_copy_passes(tmp_path):
+    oracle.lib()
+    assert _battery(oracle) is None
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(os.path.join(obuild.HERE, "oracle.cpp")).read()
+    assert src.count(old) >= 1, "mutation site not found: " + name
+    shutil.copy(os.path.join(obuild.HERE, "oracle.h"), tmp_path / "oracle.h")
+    (tmp_path / "oracle.cpp").write_text(src.replace(old, new))
+    so = str(tmp_path / ("lib_%s.so" % name))
+    subprocess.check_call(["g++"] + obuild.FLAGS + [str(tmp_path / "oracle.cpp"), "-o", so])
+    lib = _load(so)
+    with _Swap(lib) as orc:
+        failed = _battery(orc)
+    assert failed is not None, "mutant %s passed every pin" % name
