@@ -1,0 +1,369 @@
+"""Benchmark of the int8 gradient-bucket path on the headline workload.
+
+Workload: W = 8 virtual ranks, one flat 25 MiB fp32 DDP bucket (6,553,600 elements) per
+rank, Laplace(0, 1e-4) values with 30% exact zeros and 0.1% outliers x100, dynamic_chunk
+into 200 chunks of 32,768, ring-order int8 dequantise-sum, mean.  A step is one pass of the
+whole path: the chunk table (gq_plan_chunks) and the fused quantise + reduce
+(gq_fused_allreduce_sim) over one input set.  Steps rotate over input sets whose total is
+several times the 129 MB L2, so every step reads its gradients from HBM.
+
+Metric: input GB/s = W * n * 4 bytes per step / step time (the fused kernel also writes
+n * 4 bytes of output, reported in the roofline traffic).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gq|reference]
+
+For N > 1 it runs under torch.distributed.run, one process per GPU: every rank runs its own
+independent copy of the workload (weak scaling, no collective on the data path), and rank 0
+prints the whole-job figure over the slowest rank.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+W = 8
+N_ELEMS = 6553600
+ELEM_BYTES = 4
+IN_BYTES = W * N_ELEMS * ELEM_BYTES          # 209,715,200
+OUT_BYTES = N_ELEMS * 4                      # 26,214,400
+INPUT_SETS = 4                               # 839 MB rotated
+METRIC = "fused quantize+reduce input GB/s at W=8, 25 MB fp32 bucket; % of GB300 HBM peak"
+WORKLOAD = "W=8 virtual ranks x 25 MiB fp32 bucket (6,553,600 elem), Laplace(0,1e-4) 30% zeros 0.1% x100, ring order"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", default="gq", choices=["gq", "reference"])
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length (cpu_baseline)")
+    return p.parse_args()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        rows = self.rows
+        if self.window:
+            inside = [r for r in rows if self.window[0] - 0.15 <= r[0] <= self.window[1] + 0.15]
+            rows = inside or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1][0]) for r in rows if r[1][0].replace(".", "").isdigit()]
+        mx = [float(r[1][1]) for r in rows if r[1][1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if len(r[1]) > 3 + k and "Active" in r[1][3 + k]
+                          and "Not" not in r[1][3 + k]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(seconds, host_rows, stride, offsets):
+    """The oracle (single-threaded C++), repeated full passes of the workload until at least
+    `seconds` have elapsed.  Returns (GB/s of input, passes, elapsed)."""
+    import oracle
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.fused(host_rows, W, stride, offsets, oracle.RING)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return passes * IN_BYTES / el / 1e9, passes, el
+
+
+def _chunk_rows(host, stride, offsets, j0, j1):
+    """Rows of chunks [j0, j1) of the workload, rebased to a table starting at 0."""
+    lo, hi = int(offsets[j0]), int(offsets[j1])
+    n = hi - lo
+    s2 = -(-n // 4) * 4
+    rows = np.zeros(W * s2, dtype=np.float32)
+    for r in range(W):
+        rows[r * s2:r * s2 + n] = host[r * stride + lo:r * stride + hi]
+    return rows, s2, offsets[j0:j1 + 1] - lo
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores, same metric and workload.  Each step is a
+    bounded sample: a window of consecutive chunks (all 8 ranks), sized from a measured
+    per-chunk time so the whole run takes about two minutes."""
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    import workloads as wl
+    host, stride = wl.rows(2, W, N_ELEMS)
+    offsets = oracle.plan_chunks([N_ELEMS], 4)
+    nc = len(offsets) - 1
+    rows, s2, off = _chunk_rows(host, stride, offsets, 0, 1)
+    t0 = time.perf_counter()
+    oracle.fused(rows, W, s2, off, oracle.RING)
+    per_chunk = max(time.perf_counter() - t0, 1e-4)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    cps = int(min(nc, max(1, budget // per_chunk)))
+    windows = [_chunk_rows(host, stride, offsets, j, min(nc, j + cps)) for j in range(0, nc, cps)]
+    in_bytes = [W * int(o[-1]) * ELEM_BYTES for _, _, o in windows]
+    for k in range(args.warmup):
+        r_, s_, o_ = windows[k % len(windows)]
+        oracle.fused(r_, W, s_, o_, oracle.RING)
+    done, t0 = 0, time.perf_counter()
+    for k in range(args.steps):
+        r_, s_, o_ = windows[k % len(windows)]
+        oracle.plan_chunks([N_ELEMS], 4)
+        oracle.fused(r_, W, s_, o_, oracle.RING)
+        done += in_bytes[k % len(windows)]
+    el = time.perf_counter() - t0
+    value = done / el / 1e9
+    sample = "%d consecutive chunks of 32,768 x 8 ranks per step (of 200 in the 25 MiB bucket), ring" % cps
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "order": "ring"},
+            "cpu_baseline": {"kind": "oracle", "value": value, "unit": "GB/s", "cores": 1, "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gq(args):
+    import torch
+    ws, rank, local = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import dp_gradient_bucket_gb300 as gq
+    import workloads as wl
+
+    host, stride = wl.rows(2, W, N_ELEMS)
+    eb = ELEM_BYTES
+    # input sets: the generated bucket and copies with each rank's rows rotated, so every set
+    # is a distinct 210 MB region holding the same values
+    sets = []
+    base = torch.from_numpy(host).to(dev)
+    for k in range(INPUT_SETS):
+        sets.append(base.view(W, stride).roll(k, dims=0).reshape(-1).contiguous())
+    del base
+    nc = gq.gq_plan_chunks([N_ELEMS], eb)
+    offsets = torch.empty(nc + 1, dtype=torch.int64, device=dev)
+    out = torch.empty(N_ELEMS, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(k):
+        gq.gq_plan_chunks([N_ELEMS], eb, offsets, stream)
+        gq.gq_fused_allreduce_sim(sets[k % INPUT_SETS], W, stride, offsets, nc, 1.0, "ring", out, stream=stream)
+
+    for k in range(max(args.warmup, 3)):
+        step(k)
+    st = gq.gq_get_error(stream)
+    if st != gq.GQ_OK:
+        raise RuntimeError("device error before timing: " + gq.gq_status_string(st))
+
+    # timed region: K steps; per-launch events around the fused kernel on its stream
+    ev_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    t_all0.record(stream)
+    for k in range(args.steps):
+        gq.gq_plan_chunks([N_ELEMS], eb, offsets, stream)
+        ev_start[k].record(stream)
+        gq.gq_fused_allreduce_sim(sets[k % INPUT_SETS], W, stride, offsets, nc, 1.0, "ring", out, stream=stream)
+        ev_end[k].record(stream)
+    t_all1.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier(ws)
+    clocks.mark(w0, w1)
+    time.sleep(0.25)
+    clocks.stop()
+    st = gq.gq_get_error(stream)
+    if st != gq.GQ_OK:
+        raise RuntimeError("device error in timed region: " + gq.gq_status_string(st))
+    total_ms = t_all0.elapsed_time(t_all1)
+    kern_ms = [a.elapsed_time(b) for a, b in zip(ev_start, ev_end)]
+    kern_avg_ms = sum(kern_ms) / len(kern_ms)
+    step_ms = max_over_ranks(total_ms / args.steps, ws)
+    value = ws * IN_BYTES / (step_ms * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers: pinned host rows -> device, plan,
+    # fused, output -> pinned host, every step
+    pinned_in = torch.from_numpy(host).pin_memory()
+    pinned_out = torch.empty(N_ELEMS, dtype=torch.float32).pin_memory()
+    dev_in = torch.empty_like(sets[0])
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        dev_in.copy_(pinned_in, non_blocking=True)
+        gq.gq_plan_chunks([N_ELEMS], eb, offsets, stream)
+        gq.gq_fused_allreduce_sim(dev_in, W, stride, offsets, nc, 1.0, "ring", out, stream=stream)
+        pinned_out.copy_(out, non_blocking=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dev_in.copy_(pinned_in, non_blocking=True)
+        gq.gq_plan_chunks([N_ELEMS], eb, offsets, stream)
+        gq.gq_fused_allreduce_sim(dev_in, W, stride, offsets, nc, 1.0, "ring", out, stream=stream)
+        pinned_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws)
+    e2e_value = ws * IN_BYTES / (e2e_ms * 1e-3) / 1e9
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks["hbm_gbs"])
+    alg_bytes = IN_BYTES + OUT_BYTES
+    achieved = alg_bytes / (kern_avg_ms * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "fused_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            with open(tpath) as f:
+                tj = json.load(f)
+            if tj.get("kernel_source_hash") == kernel_source_hash():
+                traffic = tj.get("dram_bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+
+    import oracle  # cpu_baseline leg only
+    offs_host = oracle.plan_chunks([N_ELEMS], 4)
+    cpu_gbs, passes, el = oracle_sample(args.cpu_seconds, host, stride, offs_host)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "order": "ring", "chunks": nc, "input_bytes_per_step": IN_BYTES,
+                   "l2": "%d rotating input sets of %d MB (> 129 MB L2)" % (INPUT_SETS, IN_BYTES // 10 ** 6),
+                   "step": "gq_plan_chunks + gq_fused_allreduce_sim"},
+        "hbm_peak_fraction": value / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "kernel": "k_fused<f32>", "kernel_avg_us": kern_avg_ms * 1e3,
+                     "algorithmic_bytes_per_launch": alg_bytes, "peak_source": peak_kind},
+        "cpu_baseline": {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d full passes of the workload (8 x 6,553,600 fp32, ring) in %.1f s" % (
+                             passes, el)},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": IN_BYTES,
+                "d2h_bytes_per_step": OUT_BYTES},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gq_kernels.cu", "gq_device.cuh"):
+        with open(os.path.join(ROOT, "dp_gradient_bucket_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gq(args)
+
+
+if __name__ == "__main__":
+    main()

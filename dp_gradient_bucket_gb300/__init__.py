@@ -1,0 +1,162 @@
+"""Python binding of libgq.so (include/gq.h): int8 gradient-bucket quantise + W-way reduce.
+
+Argument marshalling only.  Every step of the path runs in the library's CUDA kernels;
+PyTorch is used for device memory and streams.  There is no fallback: if libgq.so is
+missing or fails to load, importing the binding raises.
+
+Functions keep the C names: gq_plan_buckets, gq_plan_chunks, gq_quantize,
+gq_reduce_dequant, gq_fused_allreduce_sim, gq_get_error, gq_status_string.  Device
+arguments are CUDA torch tensors (contiguous; their storage is used as is); `stream` is a
+torch.cuda.Stream, a raw cudaStream_t integer, or None for torch's current stream.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgq.so")
+
+GQ_OK = 0
+GQ_ERR_INVALID_ARG = 1
+GQ_ERR_MISALIGNED = 2
+GQ_ERR_CUDA = 3
+GQ_ERR_TIMEOUT = 4
+GQ_ERR_UNSUPPORTED = 5
+GQ_WARN_NONFINITE = 6
+GQ_ERR_BAD_TABLE = 7
+
+GQ_F32, GQ_F16 = 0, 1
+GQ_ORDER_SEQ, GQ_ORDER_RING, GQ_ORDER_TREE = 0, 1, 2
+ORDERS = {"seq": GQ_ORDER_SEQ, "ring": GQ_ORDER_RING, "tree": GQ_ORDER_TREE}
+GQ_MAX_RANKS = 64
+GQ_DEFAULT_BUCKET_CAP_BYTES = 25 * 1024 * 1024
+
+
+class GQError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s" % (where, gq_status_string(status)))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libgq.so is not built: run `python -c 'import __graft_entry__ as g; g.build()'` "
+                          "(expected at %s)" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    sz, p, i32, i64 = ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    L.gq_plan_buckets.argtypes = [p, sz, sz, sz, p, p, sz, p]
+    L.gq_plan_chunks.argtypes = [p, sz, sz, p, sz, p, p]
+    L.gq_quantize.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, p, p, p]
+    L.gq_reduce_dequant.argtypes = [p, p, i32, sz, p, sz, i32, p, p]
+    L.gq_fused_allreduce_sim.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p]
+    L.gq_get_error.argtypes = [p]
+    L.gq_status_string.argtypes = [i32]
+    L.gq_status_string.restype = ctypes.c_char_p
+    for name in ("gq_plan_buckets", "gq_plan_chunks", "gq_quantize", "gq_reduce_dequant",
+                 "gq_fused_allreduce_sim", "gq_get_error"):
+        getattr(L, name).restype = i32
+    return L
+
+
+lib = _load()
+
+
+def gq_status_string(status):
+    return lib.gq_status_string(int(status)).decode()
+
+
+def _check(status, where):
+    if status != GQ_OK:
+        raise GQError(status, where)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return GQ_F32
+    if t.dtype == torch.float16:
+        return GQ_F16
+    raise TypeError("gradients must be float32 or float16, got %s" % t.dtype)
+
+
+def gq_plan_buckets(tensor_elems, elem_bytes, cap_bytes=GQ_DEFAULT_BUCKET_CAP_BYTES):
+    """Host-side bucket assignment -> (bucket_of_tensor int32[T], bucket_elems int64[B])."""
+    te = np.ascontiguousarray(tensor_elems, dtype=np.uint64)
+    nb = ctypes.c_size_t(0)
+    st = lib.gq_plan_buckets(te.ctypes.data if te.size else None, te.size, elem_bytes, cap_bytes,
+                             None, None, 0, ctypes.byref(nb))
+    if st != GQ_OK and nb.value == 0 and te.size:
+        _check(st, "gq_plan_buckets")
+    bot = np.zeros(max(te.size, 1), dtype=np.int32)
+    be = np.zeros(max(nb.value, 1), dtype=np.uint64)
+    st = lib.gq_plan_buckets(te.ctypes.data if te.size else None, te.size, elem_bytes, cap_bytes,
+                             bot.ctypes.data, be.ctypes.data, be.size, ctypes.byref(nb))
+    _check(st, "gq_plan_buckets")
+    return bot[:te.size].copy(), be[:nb.value].astype(np.int64)
+
+
+def gq_plan_chunks(bucket_elems, elem_bytes, d_offsets=None, stream=None):
+    """Chunk count of buckets laid end to end; fills the device table d_offsets (int64
+    CUDA tensor of at least num_chunks + 1 entries) on `stream` when given."""
+    be = np.ascontiguousarray(bucket_elems, dtype=np.uint64)
+    n = ctypes.c_size_t(0)
+    if d_offsets is not None:
+        import torch
+        if d_offsets.dtype != torch.int64:
+            raise TypeError("offsets must be int64")
+    st = lib.gq_plan_chunks(be.ctypes.data, be.size, elem_bytes, _dptr(d_offsets),
+                            0 if d_offsets is None else d_offsets.numel(), ctypes.byref(n),
+                            _stream(stream) if d_offsets is not None else None)
+    _check(st, "gq_plan_chunks")
+    return n.value
+
+
+def gq_quantize(grads, W, rank_stride, d_offsets, num_chunks, loss_scale, codes, scales, stream=None):
+    st = lib.gq_quantize(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets), num_chunks,
+                         loss_scale, _dptr(codes), _dptr(scales), _stream(stream))
+    _check(st, "gq_quantize")
+
+
+def gq_reduce_dequant(codes, scales, W, rank_stride, d_offsets, num_chunks, order, out, stream=None):
+    st = lib.gq_reduce_dequant(_dptr(codes), _dptr(scales), W, rank_stride, _dptr(d_offsets), num_chunks,
+                               ORDERS.get(order, order), _dptr(out), _stream(stream))
+    _check(st, "gq_reduce_dequant")
+
+
+def gq_fused_allreduce_sim(grads, W, rank_stride, d_offsets, num_chunks, loss_scale, order, out,
+                           codes=None, scales=None, stream=None):
+    st = lib.gq_fused_allreduce_sim(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
+                                    num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out),
+                                    _dptr(codes), _dptr(scales), _stream(stream))
+    _check(st, "gq_fused_allreduce_sim")
+
+
+def gq_get_error(stream=None):
+    """Waits for the stream; returns (and clears) the device error status."""
+    return lib.gq_get_error(_stream(stream))
+
+
+def row_stride(n, elem_bytes):
+    """Smallest rank_stride >= n (and >= 1 group) whose rows start on 16-byte boundaries."""
+    per = 16 // elem_bytes
+    return max(per, -(-int(n) // per) * per)

@@ -1,0 +1,231 @@
+// gq_api.cu -- the C ABI declared in include/gq.h: argument checks, then one launch.
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/gq.h"
+#include "gq_internal.h"
+
+namespace {
+
+// dynamic_chunk ("pipelined HCCL AllReduce" article, §2.1): 128 KiB base size, 64-byte
+// alignment; the divisor is 128 KiB minus 128 KiB mod 64.
+constexpr uint64_t kChunkSize = 128 * 1024;
+constexpr uint64_t kAlignment = 64;
+constexpr uint64_t kDivisor = kChunkSize - kChunkSize % kAlignment;
+
+struct BucketPlan {
+    uint64_t piece;  // torch.chunk piece length (0 for an empty bucket)
+    uint64_t count;  // chunks
+};
+
+BucketPlan plan_one(uint64_t n, uint64_t eb) {
+    if (n == 0) return {0, 1};  // torch.chunk of an empty tensor: one empty piece
+    uint64_t k = n * eb / kDivisor;
+    if (k < 1) k = 1;
+    const uint64_t c = (n + k - 1) / k;
+    return {c, (n + c - 1) / c};
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return abytes && bbytes && a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+gq_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return GQ_OK;
+    if (e == cudaErrorNotSupported || e == cudaErrorInvalidDeviceFunction || e == cudaErrorNoKernelImageForDevice ||
+        e == cudaErrorInvalidClusterSize)
+        return GQ_ERR_UNSUPPORTED;
+    return GQ_ERR_CUDA;
+}
+
+size_t elem_bytes_of(gq_dtype dt) { return dt == GQ_F16 ? 2 : 4; }
+
+// Checks shared by gq_quantize and gq_fused_allreduce_sim.
+gq_status check_grads(const void* d_grads, gq_dtype dt, int W, size_t rank_stride, const int64_t* d_offsets,
+                      size_t num_chunks, float loss_scale) {
+    if (!d_grads || !d_offsets) return GQ_ERR_INVALID_ARG;
+    if (dt != GQ_F32 && dt != GQ_F16) return GQ_ERR_INVALID_ARG;
+    if (W < 1 || W > GQ_MAX_RANKS) return GQ_ERR_INVALID_ARG;
+    if (num_chunks < 1 || num_chunks > static_cast<size_t>(INT_MAX) / 16) return GQ_ERR_INVALID_ARG;
+    if (!(loss_scale > 0.0f) || !std::isfinite(loss_scale)) return GQ_ERR_INVALID_ARG;
+    if (rank_stride > (static_cast<size_t>(1) << 40)) return GQ_ERR_INVALID_ARG;
+    if (!aligned(d_grads, 16) || !aligned(d_offsets, 8)) return GQ_ERR_MISALIGNED;
+    if ((rank_stride * elem_bytes_of(dt)) % 16 != 0) return GQ_ERR_MISALIGNED;
+    return GQ_OK;
+}
+
+gq::QuantArgs quant_args(const void* d_grads, gq_dtype dt, int W, size_t rank_stride, const int64_t* d_offsets,
+                         size_t num_chunks, float loss_scale) {
+    gq::QuantArgs a;
+    a.grads = d_grads;
+    a.dt = dt == GQ_F16 ? 1 : 0;
+    a.W = W;
+    a.rank_stride = static_cast<int64_t>(rank_stride);
+    a.offsets = d_offsets;
+    a.num_chunks = static_cast<int64_t>(num_chunks);
+    a.inv = static_cast<float>(1.0 / static_cast<double>(loss_scale));
+    a.scaled = a.inv != 1.0f;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+gq_status gq_plan_buckets(const size_t* tensor_elems, size_t num_tensors, size_t elem_bytes, size_t cap_bytes,
+                          int32_t* bucket_of_tensor, size_t* bucket_elems, size_t bucket_capacity,
+                          size_t* num_buckets_out) {
+    if (!num_buckets_out || (num_tensors && !tensor_elems) || (bucket_capacity && !bucket_elems))
+        return GQ_ERR_INVALID_ARG;
+    if ((elem_bytes != 2 && elem_bytes != 4) || cap_bytes == 0) return GQ_ERR_INVALID_ARG;
+    // First pass: count, so nothing is written when the capacity is short.
+    size_t nb = 0, open = 0;
+    for (size_t t = 0; t < num_tensors; ++t) {
+        if (tensor_elems[t] > (SIZE_MAX / 8)) return GQ_ERR_INVALID_ARG;
+        const size_t bytes = tensor_elems[t] * elem_bytes;
+        if (nb == 0 || (open > 0 && open + bytes > cap_bytes)) {
+            ++nb;
+            open = 0;
+        }
+        open += bytes;
+    }
+    *num_buckets_out = nb;
+    if (nb > bucket_capacity) return GQ_ERR_INVALID_ARG;
+    nb = 0;
+    open = 0;
+    for (size_t t = 0; t < num_tensors; ++t) {
+        const size_t bytes = tensor_elems[t] * elem_bytes;
+        if (nb == 0 || (open > 0 && open + bytes > cap_bytes)) {
+            bucket_elems[nb++] = 0;
+            open = 0;
+        }
+        if (bucket_of_tensor) bucket_of_tensor[t] = static_cast<int32_t>(nb - 1);
+        bucket_elems[nb - 1] += tensor_elems[t];
+        open += bytes;
+    }
+    return GQ_OK;
+}
+
+gq_status gq_plan_chunks(const size_t* bucket_elems, size_t num_buckets, size_t elem_bytes, int64_t* d_offsets,
+                         size_t offsets_capacity, size_t* num_chunks_out, gq_stream_t stream) {
+    if (!bucket_elems || !num_chunks_out || num_buckets == 0) return GQ_ERR_INVALID_ARG;
+    if (elem_bytes != 2 && elem_bytes != 4) return GQ_ERR_INVALID_ARG;
+    std::vector<gq::PlanBucket> plan(num_buckets);
+    uint64_t total_chunks = 0, start = 0;
+    for (size_t b = 0; b < num_buckets; ++b) {
+        if (bucket_elems[b] > (static_cast<uint64_t>(1) << 40)) return GQ_ERR_INVALID_ARG;
+        const BucketPlan bp = plan_one(bucket_elems[b], elem_bytes);
+        plan[b].elem_start = static_cast<int64_t>(start);
+        plan[b].chunk_start = static_cast<int64_t>(total_chunks);
+        plan[b].piece = static_cast<int64_t>(bp.piece);
+        plan[b].count = static_cast<int64_t>(bp.count);
+        total_chunks += bp.count;
+        start += bucket_elems[b];
+    }
+    *num_chunks_out = static_cast<size_t>(total_chunks);
+    if (!d_offsets) return GQ_OK;
+    if (offsets_capacity < total_chunks + 1) return GQ_ERR_INVALID_ARG;
+    if (!aligned(d_offsets, 8)) return GQ_ERR_MISALIGNED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (size_t b0 = 0; b0 < num_buckets; b0 += gq::kPlanBucketsPerLaunch) {
+        const size_t nb = num_buckets - b0 < static_cast<size_t>(gq::kPlanBucketsPerLaunch)
+                              ? num_buckets - b0
+                              : static_cast<size_t>(gq::kPlanBucketsPerLaunch);
+        const bool last = b0 + nb == num_buckets;
+        const cudaError_t e = gq::launch_plan(plan.data() + b0, static_cast<int>(nb), d_offsets,
+                                              last ? static_cast<int64_t>(total_chunks) : -1,
+                                              static_cast<int64_t>(start), s);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    return GQ_OK;
+}
+
+gq_status gq_quantize(const void* d_grads, gq_dtype dt, int W, size_t rank_stride, const int64_t* d_offsets,
+                      size_t num_chunks, float loss_scale, int8_t* d_codes, float* d_scales, gq_stream_t stream) {
+    gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
+    if (st != GQ_OK) return st;
+    if (!d_codes || !d_scales) return GQ_ERR_INVALID_ARG;
+    if (!aligned(d_codes, 16) || !aligned(d_scales, 4)) return GQ_ERR_MISALIGNED;
+    const size_t gbytes = static_cast<size_t>(W) * rank_stride * elem_bytes_of(dt);
+    if (overlaps(d_grads, gbytes, d_codes, static_cast<size_t>(W) * rank_stride) ||
+        overlaps(d_grads, gbytes, d_scales, static_cast<size_t>(W) * num_chunks * 4) ||
+        overlaps(d_codes, static_cast<size_t>(W) * rank_stride, d_scales, static_cast<size_t>(W) * num_chunks * 4))
+        return GQ_ERR_INVALID_ARG;
+    const gq::QuantArgs a = quant_args(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
+    return from_cuda(gq::launch_quantize(a, d_codes, d_scales, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gq_status gq_reduce_dequant(const int8_t* d_codes, const float* d_scales, int W, size_t rank_stride,
+                            const int64_t* d_offsets, size_t num_chunks, gq_order order, float* d_out,
+                            gq_stream_t stream) {
+    if (!d_codes || !d_scales || !d_offsets || !d_out) return GQ_ERR_INVALID_ARG;
+    if (W < 1 || W > GQ_MAX_RANKS) return GQ_ERR_INVALID_ARG;
+    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (num_chunks < 1 || num_chunks > static_cast<size_t>(INT_MAX)) return GQ_ERR_INVALID_ARG;
+    if (rank_stride > (static_cast<size_t>(1) << 40)) return GQ_ERR_INVALID_ARG;
+    if (!aligned(d_codes, 16) || !aligned(d_out, 16) || !aligned(d_scales, 4) || !aligned(d_offsets, 8))
+        return GQ_ERR_MISALIGNED;
+    if (rank_stride % 4 != 0) return GQ_ERR_MISALIGNED;
+    const size_t cbytes = static_cast<size_t>(W) * rank_stride;
+    if (overlaps(d_out, rank_stride * 4, d_codes, cbytes) ||
+        overlaps(d_out, rank_stride * 4, d_scales, static_cast<size_t>(W) * num_chunks * 4))
+        return GQ_ERR_INVALID_ARG;
+    return from_cuda(gq::launch_reduce(d_codes, d_scales, W, static_cast<int64_t>(rank_stride), d_offsets,
+                                       static_cast<int64_t>(num_chunks), static_cast<int>(order), d_out,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gq_status gq_fused_allreduce_sim(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                 const int64_t* d_offsets, size_t num_chunks, float loss_scale, gq_order order,
+                                 float* d_out, int8_t* d_codes_opt, float* d_scales_opt, gq_stream_t stream) {
+    gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
+    if (st != GQ_OK) return st;
+    if (!d_out) return GQ_ERR_INVALID_ARG;
+    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (!aligned(d_out, 16) || (d_codes_opt && !aligned(d_codes_opt, 16)) ||
+        (d_scales_opt && !aligned(d_scales_opt, 4)))
+        return GQ_ERR_MISALIGNED;
+    const size_t gbytes = static_cast<size_t>(W) * rank_stride * elem_bytes_of(dt);
+    const size_t obytes = rank_stride * 4, cbytes = d_codes_opt ? static_cast<size_t>(W) * rank_stride : 0,
+                 sbytes = d_scales_opt ? static_cast<size_t>(W) * num_chunks * 4 : 0;
+    if (overlaps(d_grads, gbytes, d_out, obytes) || overlaps(d_grads, gbytes, d_codes_opt, cbytes) ||
+        overlaps(d_grads, gbytes, d_scales_opt, sbytes) || overlaps(d_out, obytes, d_codes_opt, cbytes) ||
+        overlaps(d_out, obytes, d_scales_opt, sbytes) || overlaps(d_codes_opt, cbytes, d_scales_opt, sbytes))
+        return GQ_ERR_INVALID_ARG;
+    const gq::QuantArgs a = quant_args(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
+    return from_cuda(gq::launch_fused(a, static_cast<int>(order), d_out, d_codes_opt, d_scales_opt,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gq_status gq_get_error(gq_stream_t stream) {
+    unsigned w = 0;
+    const cudaError_t e = gq::read_and_clear_error_word(&w, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return GQ_ERR_CUDA;
+    if (w & gq::kErrTimeout) return GQ_ERR_TIMEOUT;
+    if (w & gq::kErrBadTable) return GQ_ERR_BAD_TABLE;
+    if (w & gq::kErrNonfinite) return GQ_WARN_NONFINITE;
+    return GQ_OK;
+}
+
+const char* gq_status_string(gq_status s) {
+    switch (s) {
+        case GQ_OK: return "GQ_OK";
+        case GQ_ERR_INVALID_ARG: return "GQ_ERR_INVALID_ARG: bad argument";
+        case GQ_ERR_MISALIGNED: return "GQ_ERR_MISALIGNED: pointer or row start not 16-byte aligned";
+        case GQ_ERR_CUDA: return "GQ_ERR_CUDA: a CUDA runtime call failed";
+        case GQ_ERR_TIMEOUT: return "GQ_ERR_TIMEOUT: a device-side bounded wait gave up";
+        case GQ_ERR_UNSUPPORTED: return "GQ_ERR_UNSUPPORTED: device cannot run this kernel";
+        case GQ_WARN_NONFINITE: return "GQ_WARN_NONFINITE: an input value was Inf or NaN";
+        case GQ_ERR_BAD_TABLE: return "GQ_ERR_BAD_TABLE: a chunk table broke its rules";
+    }
+    return "unknown gq_status";
+}
+
+}  // extern "C"

@@ -1,0 +1,249 @@
+// gq_device.cuh -- device helpers for the int8 gradient-bucket kernels (sm_103a).
+//
+// Inline PTX for the Blackwell data-movement pieces (mbarrier, bulk async copy into
+// shared memory, thread-block-cluster barriers and distributed shared memory), and the
+// quantiser arithmetic.  All floating point is written with the round-to-nearest
+// intrinsics (__fmul_rn, __fadd_rn, __fsub_rn, __fdiv_rn): they are never fused into
+// FMA, so every step is one binary32 operation.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace gq {
+
+constexpr int kMaxRanks = 64;
+
+// ---------------------------------------------------------------- shared memory / mbarrier
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Make mbarrier initialisation visible to the async (TMA) proxy before any copy uses it.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on an mbarrier phase: gives up after `limit_ns` of wall time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Bulk async copy global -> this CTA's shared memory, completing `bytes` of transaction
+// count on `bar`.  dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------- thread-block clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Load a u32 from the same shared-memory variable in CTA `cta` of this cluster.
+__device__ __forceinline__ uint32_t dsmem_load_u32(const void* local, uint32_t cta) {
+    uint32_t remote, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(cta));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------- loads
+
+struct alignas(16) V16 {
+    uint32_t w[4];
+};
+
+__device__ __forceinline__ V16 ld_global_nc_v16(const void* p) {
+    V16 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ V16 ld_shared_v16(const void* p) {
+    V16 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
+// Element e of a 16-byte group as float (fp32: 4 per group; fp16: 8 per group, exact widening).
+template <int DT>
+__device__ __forceinline__ float group_elem(const V16& v, int e);
+
+template <>
+__device__ __forceinline__ float group_elem<0>(const V16& v, int e) {
+    return __uint_as_float(v.w[e]);
+}
+
+template <>
+__device__ __forceinline__ float group_elem<1>(const V16& v, int e) {
+    const uint32_t w = v.w[e >> 1];
+    const unsigned short h = static_cast<unsigned short>((e & 1) ? (w >> 16) : (w & 0xffffu));
+    return __half2float(__ushort_as_half(h));
+}
+
+// |x| bit pattern of element e, ordered like |x| for finite values (fp32: 31 bits, fp16: 15).
+template <int DT>
+__device__ __forceinline__ uint32_t group_abs_bits(const V16& v, int e);
+
+template <>
+__device__ __forceinline__ uint32_t group_abs_bits<0>(const V16& v, int e) {
+    return v.w[e] & 0x7fffffffu;
+}
+
+template <>
+__device__ __forceinline__ uint32_t group_abs_bits<1>(const V16& v, int e) {
+    const uint32_t w = v.w[e >> 1];
+    return ((e & 1) ? (w >> 16) : w) & 0x7fffu;
+}
+
+// ---------------------------------------------------------------- quantiser arithmetic
+
+// Adding 1.5 * 2^23 to |t| < 2^22 leaves the integer rne(t) in the low mantissa bits:
+// u = M + rne(t) exactly, so rne(t) = u - M exactly and its low byte is the int8 code.
+constexpr float kMagic = 12582912.0f;
+// Quotients this close to a half-integer are re-decided with the exact IEEE division.
+constexpr float kNearTie = 0.49993896484375f;  // 0.5 - 2^-14
+
+// Per-(rank, chunk) scale state.
+//   mode 0: s == 0 (all-zero chunk or underflowed scale): every code is 0.
+//   mode 1: s a normal number: t = g * rcp(s) decides rne(g / s) unless t lies within
+//           2^-14 of a half-integer.  Bound: rcp and the product each round with relative
+//           error <= 2^-24 and |g / s| <= 127 * (1 + 2^-23), so |t - g/s| < 2^-16, and the
+//           correctly rounded quotient lies within 2^-17 of g/s; a t at least 2^-14 away
+//           from every half-integer therefore has the same nearest integer as fl(g / s).
+//   mode 2: s subnormal: its relative error can be large, |g / s| may pass 127.5, so the
+//           exact division and the clamp to [-128, 127] are always taken.
+struct ScaleQ {
+    float s;
+    float rcp;
+    int mode;
+};
+
+__device__ __forceinline__ ScaleQ make_scale(float m) {
+    ScaleQ q;
+    q.s = __fdiv_rn(m, 127.0f);  // scale = max|g| / 127.0
+    q.rcp = 0.0f;
+    if (q.s == 0.0f) {
+        q.mode = 0;
+    } else if (q.s >= 1.17549435e-38f) {
+        q.mode = 1;
+        q.rcp = __frcp_rn(q.s);
+    } else {
+        q.mode = 2;
+    }
+    return q;
+}
+
+// Returns u = M + q, q = clamp(rne(fl(g / s)), -128, 127) (q = 0 when s == 0).
+__device__ __forceinline__ float quant_u(float g, const ScaleQ& sq) {
+    if (sq.mode == 1) {
+        const float t = __fmul_rn(g, sq.rcp);
+        float u = __fadd_rn(t, kMagic);
+        const float d = __fsub_rn(t, __fsub_rn(u, kMagic));  // t - rne(t), exact
+        if (fabsf(d) > kNearTie) u = __fadd_rn(__fdiv_rn(g, sq.s), kMagic);
+        return u;
+    }
+    if (sq.mode == 2) {
+        const float y = fminf(fmaxf(__fdiv_rn(g, sq.s), -128.0f), 127.0f);
+        return __fadd_rn(y, kMagic);
+    }
+    return kMagic;
+}
+
+__device__ __forceinline__ float code_value(float u) { return __fsub_rn(u, kMagic); }
+__device__ __forceinline__ uint32_t code_byte(float u) { return __float_as_uint(u) & 0xffu; }
+
+// Binary-counter form of the pairwise tree over ranks in index order: leaf r merges with
+// the complete subtrees whose sizes are the trailing one-bits of r; at the end the pending
+// subtrees are folded from the smallest (rightmost) up.  This pairs exactly as the
+// level-by-level rule "(0+1), (2+3), ..., odd one carried" does.
+struct TreeAcc {
+    float st[7];
+    uint32_t count;
+    __device__ __forceinline__ void init() { count = 0; }
+    __device__ __forceinline__ void push(float x) {
+        uint32_t c = count;
+        int k = 0;
+#pragma unroll
+        for (int b = 0; b < 7; ++b) {
+            if (c & 1u) {
+                x = __fadd_rn(st[b], x);
+                k = b + 1;
+                c >>= 1;
+            } else {
+                break;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < 7; ++b)
+            if (b == k) st[b] = x;
+        ++count;
+    }
+    __device__ __forceinline__ float result() const {
+        float acc = 0.0f;
+        bool have = false;
+#pragma unroll
+        for (int b = 0; b < 7; ++b) {
+            if (count & (1u << b)) {
+                acc = have ? __fadd_rn(st[b], acc) : st[b];
+                have = true;
+            }
+        }
+        return acc;
+    }
+};
+
+}  // namespace gq

@@ -1,0 +1,54 @@
+// gq_internal.h -- host-side launchers shared by the C-ABI front end (gq_api.cu) and the
+// kernels (gq_kernels.cu).  Arguments arrive here already validated.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gq {
+
+// Device error word bits (set by kernels, read and cleared by gq_get_error).
+constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrNonfinite = 2u;
+constexpr unsigned kErrBadTable = 4u;
+
+struct PlanBucket {  // one bucket of the chunk table, as kernel arguments
+    int64_t elem_start;   // element offset of the bucket
+    int64_t chunk_start;  // index of its first chunk in the table
+    int64_t piece;        // torch.chunk piece length c (0 for an empty bucket)
+    int64_t count;        // number of chunks
+};
+
+constexpr int kPlanBucketsPerLaunch = 64;
+
+// Writes offsets[chunk_start .. chunk_start+count) for each of `nb` buckets, and, when
+// `total_chunks >= 0`, the final entry offsets[total_chunks] = end_elem.
+cudaError_t launch_plan(const PlanBucket* buckets, int nb, int64_t* d_offsets, int64_t total_chunks,
+                        int64_t end_elem, cudaStream_t stream);
+
+struct QuantArgs {
+    const void* grads;
+    int dt;  // 0 f32, 1 f16
+    int W;
+    int64_t rank_stride;
+    const int64_t* offsets;
+    int64_t num_chunks;
+    float inv;   // (float)(1 / loss_scale)
+    int scaled;  // inv != 1
+};
+
+cudaError_t launch_quantize(const QuantArgs& a, int8_t* codes, float* scales, cudaStream_t stream);
+
+cudaError_t launch_reduce(const int8_t* codes, const float* scales, int W, int64_t rank_stride,
+                          const int64_t* offsets, int64_t num_chunks, int order, float* out,
+                          cudaStream_t stream);
+
+// Returns cudaErrorNotSupported when the device cannot run cluster launches of the needed shape.
+cudaError_t launch_fused(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales,
+                         cudaStream_t stream);
+
+// Reads and clears the current device's error word (synchronous).
+cudaError_t read_and_clear_error_word(unsigned* word, cudaStream_t stream);
+
+}  // namespace gq

@@ -1,0 +1,160 @@
+/*
+ * gq.h -- int8 gradient-bucket quantise + W-way reduce on one GPU (sm_103a).
+ *
+ * The data-parallel gradient synchronisation path of the "pipelined HCCL AllReduce"
+ * article (bjdmk.com.cn/news/6235379), run over W virtual ranks whose gradient rows
+ * sit in one GPU's HBM:
+ *   1. a DDP-Reducer-style flat bucket          ("torch_npu distributed module" article,
+ *      hwcomputing.csdn.net, §2.2 component table: Reducer bucketing; §9.2 coalescing)
+ *   2. split by dynamic_chunk                    (pipelined-AllReduce article §2.1)
+ *   3. each chunk quantised to int8 with a per-(rank, chunk) absmax scale
+ *                                                (§2.2.1 quantize_gradient), after an
+ *      optional loss-scale unscale               (§6.1 mixed-precision pipeline)
+ *   4. the W ranks' codes dequantised, summed in a fixed order and averaged: the
+ *      arithmetic of INT8_ALLREDUCE             (§2.2.1; §3.1 one SUM all_reduce per
+ *      chunk; divide by the group size as in the "torchtitan-npu 3D parallel" article,
+ *      framerc.cn/news/2545645, AMP + 3D section)
+ *
+ * Conventions shared by every entry point
+ *   - Device pointers are plain CUDA device addresses; the caller owns every buffer.
+ *     The library allocates no device or host memory and keeps no per-call state.
+ *   - `stream` is a cudaStream_t (this header does not include the CUDA headers; the
+ *     type below is the same pointer type).  NULL is the legacy default stream.  Every
+ *     call that takes a stream only enqueues work on it and returns; nothing
+ *     synchronises except gq_get_error.
+ *   - Virtual rank r's row of elements begins at element r * rank_stride of its buffer.
+ *     Rows must start on 16-byte boundaries: base pointers 16-byte aligned and
+ *     rank_stride * elem_bytes a multiple of 16 (4 fp32 / 8 fp16 elements).
+ *   - A chunk table is num_chunks + 1 int64 element offsets into a row, non-decreasing,
+ *     offsets[0] >= 0, offsets[num_chunks] <= rank_stride; chunk j covers
+ *     [offsets[j], offsets[j+1]).  gq_plan_chunks writes one for buckets laid end to end.
+ *   - codes: int8 [W][rank_stride] (row r at r * rank_stride, entries outside the chunks
+ *     untouched); scales: float [W][num_chunks]; out: float [offsets[num_chunks]].
+ *   - Outputs must not overlap inputs or each other.
+ *   - Arithmetic is IEEE binary32, round-to-nearest-even, no contraction, subnormals
+ *     kept.  For the sequential and ring orders the output is bit-for-bit the value
+ *     defined below (the same bits on every run and every GPU).
+ *
+ * Errors
+ *   Arguments are checked before anything is enqueued: a bad argument returns
+ *   GQ_ERR_INVALID_ARG (or GQ_ERR_MISALIGNED for alignment) and enqueues nothing.  A
+ *   failed launch returns GQ_ERR_CUDA.  Conditions only the device can see -- a chunk
+ *   table that breaks the rules above (those chunks are skipped), a non-finite input
+ *   value (that chunk's codes, scale and outputs are unspecified), a bounded wait that
+ *   ran out -- set bits of a per-device error word that gq_get_error reads and clears.
+ */
+#ifndef GQ_H
+#define GQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* gq_stream_t; /* == cudaStream_t */
+
+typedef enum {
+    GQ_OK = 0,
+    GQ_ERR_INVALID_ARG = 1, /* null pointer, size out of range, bad enum, table too small */
+    GQ_ERR_MISALIGNED = 2,  /* base pointer or row start not on a 16-byte boundary     */
+    GQ_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, attribute, copy)    */
+    GQ_ERR_TIMEOUT = 4,     /* a device-side bounded wait gave up (gq_get_error only)  */
+    GQ_ERR_UNSUPPORTED = 5, /* the device cannot run the kernel (not sm_103, no clusters) */
+    GQ_WARN_NONFINITE = 6,  /* an input value was Inf or NaN (gq_get_error only)       */
+    GQ_ERR_BAD_TABLE = 7    /* a chunk table broke the rules above (gq_get_error only) */
+} gq_status;
+
+typedef enum { GQ_F32 = 0, GQ_F16 = 1 } gq_dtype;
+
+/* Summation order over the W ranks for one output element.
+ *   SEQ : rank 0, 1, ..., W-1.
+ *   RING: the element's chunk is cut by torch.chunk(chunk, W) into segments of
+ *         ceil(len / W); an element of segment t is summed starting at rank (t+1) % W,
+ *         then (t+2) % W, ..., t -- the order a ring reduce-scatter accumulates in
+ *         (pipelined-AllReduce article §1, ring AllReduce).
+ *   TREE: pairwise over ranks in index order, (0+1), (2+3), ...; an odd one out is
+ *         carried up a level unchanged; repeated until one value remains.
+ * Each step is one binary32 addition acc = acc + d. */
+typedef enum { GQ_ORDER_SEQ = 0, GQ_ORDER_RING = 1, GQ_ORDER_TREE = 2 } gq_order;
+
+#define GQ_MAX_RANKS 64
+#define GQ_DEFAULT_BUCKET_CAP_BYTES ((size_t)25 * 1024 * 1024)
+
+/* Bucket assignment of a gradient list (host only, synchronous; no device work).
+ * Tensors are taken in list order; a tensor joins the open bucket unless that bucket is
+ * non-empty and the tensor would push it past cap_bytes, in which case the open bucket is
+ * closed and a new one started (so a tensor larger than the cap has a bucket of its own).
+ * Buckets are laid end to end in list order, tensors end to end within them.
+ *   tensor_elems[num_tensors]   element counts (num_tensors may be 0)
+ *   elem_bytes                  2 or 4
+ *   cap_bytes                   > 0 (GQ_DEFAULT_BUCKET_CAP_BYTES = PyTorch DDP's 25 MiB)
+ *   bucket_of_tensor[num_tensors]  out: bucket index of each tensor (may be NULL)
+ *   bucket_elems[bucket_capacity]  out: element count of each bucket
+ *   num_buckets_out             out: bucket count (written even when the capacity is short)
+ * Returns GQ_ERR_INVALID_ARG for a null required pointer, a bad size, or a bucket count
+ * above bucket_capacity (bucket_elems is then not written). */
+gq_status gq_plan_buckets(const size_t* tensor_elems, size_t num_tensors, size_t elem_bytes,
+                          size_t cap_bytes, int32_t* bucket_of_tensor, size_t* bucket_elems,
+                          size_t bucket_capacity, size_t* num_buckets_out);
+
+/* Chunk table for buckets laid end to end (pipelined-AllReduce article §2.1, dynamic_chunk):
+ * a bucket of n elements of elem_bytes gets k = max(1, n*elem_bytes // 131072) requested
+ * pieces (131072 = 128 KiB minus 128 KiB mod the 64-byte alignment), and torch.chunk
+ * semantics cut it into pieces of c = ceil(n / k) elements, the last shorter, ceil(n / c)
+ * pieces in all; an empty bucket is one empty chunk.
+ *   bucket_elems[num_buckets]  host array of bucket sizes (num_buckets >= 1)
+ *   elem_bytes                 2 or 4
+ *   d_offsets                  device array of offsets_capacity int64, or NULL to only count
+ *   num_chunks_out             out (host, written synchronously): total chunk count
+ * When d_offsets is given it receives num_chunks + 1 offsets, written by a kernel on
+ * `stream` (the bucket sizes travel as kernel arguments, so the call does not wait and
+ * can be captured in a CUDA graph).  GQ_ERR_INVALID_ARG if offsets_capacity is short. */
+gq_status gq_plan_chunks(const size_t* bucket_elems, size_t num_buckets, size_t elem_bytes,
+                         int64_t* d_offsets, size_t offsets_capacity, size_t* num_chunks_out,
+                         gq_stream_t stream);
+
+/* quantize_gradient per (rank, chunk) (pipelined-AllReduce article §2.2.1), after the
+ * optional unscale of §6.1:
+ *   g = float(x) * inv, inv = (float)(1.0 / (double)loss_scale)    (loss_scale 1: g = x)
+ *   m = max |g| over the chunk;  s = m / 127.0f;
+ *   q = s == 0 ? 0 : clamp(round_half_even(g / s), -128, 127)
+ *   d_grads   W rows of dt elements      d_codes  int8 [W][rank_stride]
+ *   d_scales  float [W][num_chunks]
+ * 1 <= W <= GQ_MAX_RANKS; loss_scale finite and > 0; num_chunks >= 1. */
+gq_status gq_quantize(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                      const int64_t* d_offsets, size_t num_chunks, float loss_scale,
+                      int8_t* d_codes, float* d_scales, gq_stream_t stream);
+
+/* INT8_ALLREDUCE arithmetic + mean (pipelined-AllReduce article §2.2.1, §3.1;
+ * 3D-parallel article, AMP + 3D section): for every element,
+ *   d_r = (float)q_r * s_r;  acc = sum of the d_r in `order`;  out = acc / (float)W. */
+gq_status gq_reduce_dequant(const int8_t* d_codes, const float* d_scales, int W,
+                            size_t rank_stride, const int64_t* d_offsets, size_t num_chunks,
+                            gq_order order, float* d_out, gq_stream_t stream);
+
+/* gq_quantize then gq_reduce_dequant in one pass over the gradients: every chunk's W rows
+ * are staged on chip once (TMA bulk copies into shared memory of a thread-block cluster
+ * that splits the chunk; the clusters exchange per-rank absmax through distributed shared
+ * memory), so the gradients are read from HBM once and the codes never leave the chip.
+ * Output bits equal those of the two calls above.  d_codes_opt / d_scales_opt, when not
+ * NULL, also receive the codes and scales. */
+gq_status gq_fused_allreduce_sim(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                 const int64_t* d_offsets, size_t num_chunks, float loss_scale,
+                                 gq_order order, float* d_out, int8_t* d_codes_opt,
+                                 float* d_scales_opt, gq_stream_t stream);
+
+/* Waits for `stream`, then reads and clears the current device's error word.  Returns
+ * GQ_OK, or the most serious recorded condition: GQ_ERR_TIMEOUT, then GQ_ERR_BAD_TABLE,
+ * then GQ_WARN_NONFINITE; GQ_ERR_CUDA if the wait or the read failed. */
+gq_status gq_get_error(gq_stream_t stream);
+
+/* Static, human-readable name of a status (never NULL). */
+const char* gq_status_string(gq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GQ_H */

@@ -1,0 +1,133 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point include/gq.h
+declares, its host-only functions (bucket plan, chunk counting, status strings) agree with
+the oracle, and bad arguments are rejected before anything is enqueued (the pointers
+below are never dereferenced: every call here fails a host-side check first)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import _golden as G
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gq():
+    import __graft_entry__
+    __graft_entry__.build()
+    import dp_gradient_bucket_gb300 as m
+    return m
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "gq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gq_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(gq):
+    names = _declared()
+    assert {"gq_plan_chunks", "gq_quantize", "gq_reduce_dequant", "gq_fused_allreduce_sim",
+            "gq_get_error", "gq_status_string", "gq_plan_buckets"} <= set(names)
+    raw = ctypes.CDLL(gq.LIB_PATH)
+    for name in names:
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(gq):
+    for code in range(8):
+        s = gq.gq_status_string(code)
+        assert s.startswith("GQ_")
+    assert gq.gq_status_string(99) == "unknown gq_status"
+
+
+def test_plan_buckets_matches_oracle(gq, orc):
+    for eb, tensors, buckets in G.bucket_cases():
+        bot, be = gq.gq_plan_buckets(tensors, eb)
+        obot, obe = orc.assign_buckets(tensors, eb)
+        assert list(be) == buckets == list(obe)
+        assert list(bot) == list(obot)
+    rng = np.random.default_rng(1)
+    for eb in (2, 4):
+        sizes = [int(x) for x in np.round(np.exp(rng.uniform(np.log(64), np.log(2359296), 500)))]
+        bot, be = gq.gq_plan_buckets(sizes, eb)
+        obot, obe = orc.assign_buckets(sizes, eb)
+        assert list(be) == list(obe) and list(bot) == list(obot)
+
+
+def test_plan_chunk_count_matches_oracle(gq, orc):
+    for n, eb, count, piece in G.chunk_sizes():
+        assert gq.gq_plan_chunks([n], eb) == count
+    rng = np.random.default_rng(2)
+    for eb in (2, 4):
+        buckets = [int(x) for x in rng.integers(0, 3_000_000, 40)] + [0, 1, 65536]
+        assert gq.gq_plan_chunks(buckets, eb) == len(orc.plan_chunks(buckets, eb)) - 1
+
+
+def _call_fused(gq, grads=0x10000, dt=0, W=8, stride=1024, offsets=0x20000, nc=4, ls=1.0, order=1,
+                out=0x30000, codes=None, scales=None):
+    return gq.lib.gq_fused_allreduce_sim(grads, dt, W, stride, offsets, nc, ls, order, out, codes, scales, None)
+
+
+def test_fused_rejects_bad_arguments(gq):
+    BAD, MIS = gq.GQ_ERR_INVALID_ARG, gq.GQ_ERR_MISALIGNED
+    assert _call_fused(gq, grads=None) == BAD
+    assert _call_fused(gq, offsets=None) == BAD
+    assert _call_fused(gq, out=None) == BAD
+    assert _call_fused(gq, W=0) == BAD
+    assert _call_fused(gq, W=65) == BAD
+    assert _call_fused(gq, dt=2) == BAD
+    assert _call_fused(gq, order=3) == BAD
+    assert _call_fused(gq, nc=0) == BAD
+    assert _call_fused(gq, ls=0.0) == BAD
+    assert _call_fused(gq, ls=-1.0) == BAD
+    assert _call_fused(gq, ls=float("inf")) == BAD
+    assert _call_fused(gq, ls=float("nan")) == BAD
+    assert _call_fused(gq, grads=0x10004) == MIS
+    assert _call_fused(gq, out=0x30008) == MIS
+    assert _call_fused(gq, offsets=0x20004) == MIS
+    assert _call_fused(gq, stride=1022) == MIS          # fp32 rows must start 16-byte aligned
+    assert _call_fused(gq, dt=1, stride=1020) == MIS    # fp16: stride multiple of 8
+    assert _call_fused(gq, codes=0x50001) == MIS
+    # out overlaps the gradient rows (8 rows x 1024 fp32 = 32 KiB from 0x10000)
+    assert _call_fused(gq, out=0x11000) == BAD
+    assert _call_fused(gq, codes=0x12000) == BAD
+
+
+def test_quantize_and_reduce_reject_bad_arguments(gq):
+    L = gq.lib
+    BAD, MIS = gq.GQ_ERR_INVALID_ARG, gq.GQ_ERR_MISALIGNED
+    assert L.gq_quantize(0x10000, 0, 8, 1024, 0x20000, 4, 1.0, None, 0x40000, None) == BAD
+    assert L.gq_quantize(0x10000, 0, 8, 1024, 0x20000, 4, 1.0, 0x40000, None, None) == BAD
+    assert L.gq_quantize(0x10000, 0, 8, 1024, 0x20000, 4, 1.0, 0x40004, 0x60000, None) == MIS
+    assert L.gq_quantize(0x10000, 0, 8, 1024, 0x20000, 4, 1.0, 0x10400, 0x60000, None) == BAD
+    assert L.gq_reduce_dequant(None, 0x1000, 8, 1024, 0x2000, 4, 1, 0x3000, None) == BAD
+    assert L.gq_reduce_dequant(0x10000, 0x1000, 8, 1024, 0x2000, 4, 7, 0x30000, None) == BAD
+    assert L.gq_reduce_dequant(0x10000, 0x1000, 8, 1022, 0x2000, 4, 1, 0x30000, None) == MIS
+    assert L.gq_reduce_dequant(0x10000, 0x1000, 8, 1024, 0x2000, 4, 1, 0x10100, None) == BAD
+
+
+def test_plan_chunks_rejects_bad_arguments(gq):
+    L = gq.lib
+    be = (ctypes.c_size_t * 2)(100, 200)
+    n = ctypes.c_size_t(0)
+    assert L.gq_plan_chunks(None, 2, 4, None, 0, ctypes.byref(n), None) == gq.GQ_ERR_INVALID_ARG
+    assert L.gq_plan_chunks(be, 0, 4, None, 0, ctypes.byref(n), None) == gq.GQ_ERR_INVALID_ARG
+    assert L.gq_plan_chunks(be, 2, 3, None, 0, ctypes.byref(n), None) == gq.GQ_ERR_INVALID_ARG
+    # table too small for 2 chunks + 1
+    assert L.gq_plan_chunks(be, 2, 4, 0x1000, 2, ctypes.byref(n), None) == gq.GQ_ERR_INVALID_ARG
+    assert n.value == 2
+    assert L.gq_plan_chunks(be, 2, 4, 0x1004, 3, ctypes.byref(n), None) == gq.GQ_ERR_MISALIGNED
+
+
+def test_plan_buckets_capacity_short(gq):
+    L = gq.lib
+    te = (ctypes.c_size_t * 3)(6553600, 6553600, 6553600)
+    be = (ctypes.c_size_t * 2)()
+    nb = ctypes.c_size_t(0)
+    assert L.gq_plan_buckets(te, 3, 4, 25 << 20, None, be, 2, ctypes.byref(nb)) == gq.GQ_ERR_INVALID_ARG
+    assert nb.value == 3
+    assert L.gq_plan_buckets(te, 3, 3, 25 << 20, None, be, 2, ctypes.byref(nb)) == gq.GQ_ERR_INVALID_ARG

@@ -1,0 +1,120 @@
+"""The kernels' arithmetic shortcuts, emulated on the CPU with IEEE binary32 numpy ops
+(each numpy float32 operation is correctly rounded, as __fmul_rn / __fadd_rn /
+__frcp_rn / __fdiv_rn are), checked against the plain definition on many inputs.
+
+1. For a normal scale s, rne(g * rcp(s)) (with the 1.5*2^23 rounding trick) equals
+   rne(fl(g / s)) whenever t = g * rcp(s) is at least 2^-14 away from a half-integer;
+   otherwise the kernel divides.
+2. The binary-counter pairwise tree pairs ranks exactly like the level-by-level rule.
+3. max|fl(x * inv)| == fl(max|x| * inv) (the absmax is taken before the unscale).
+"""
+import numpy as np
+
+M = np.float32(12582912.0)
+NEAR_TIE = np.float32(0.49993896484375)
+
+
+def kernel_codes(g, s):
+    """The kernel's mode-1 decision (s normal): returns (q, took_exact_path)."""
+    g = g.astype(np.float32)
+    rcp = np.float32(1.0) / s
+    t = g * rcp
+    u = t + M
+    d = t - (u - M)
+    near = np.abs(d) > NEAR_TIE
+    y = g / s
+    u = np.where(near, y + M, u)
+    return (u - M).astype(np.int64), near
+
+
+def reference_codes(g, s):
+    y = g.astype(np.float32) / s
+    return np.clip(np.rint(y), -128, 127).astype(np.int64)
+
+
+def test_fast_path_matches_exact_division_random():
+    rng = np.random.default_rng(0)
+    exact_taken = 0
+    for trial in range(200):
+        m = np.float32(10.0 ** rng.uniform(-36, 36))
+        s = np.float32(m / np.float32(127.0))
+        if not (s >= np.float32(2.0 ** -126)):
+            continue
+        g = (rng.uniform(-1, 1, 200000) * np.float64(m)).astype(np.float32)
+        g[0] = m
+        g[1] = -m
+        q, near = kernel_codes(g, s)
+        assert np.array_equal(q, reference_codes(g, s)), trial
+        exact_taken += int(near.sum())
+    assert exact_taken < 200 * 200000 * 1e-3
+
+
+def test_fast_path_matches_exact_division_near_ties():
+    """Values placed within a few ulp of every half-integer k + 0.5 of the quotient."""
+    rng = np.random.default_rng(1)
+    for trial in range(300):
+        m = np.float32(10.0 ** rng.uniform(-30, 30))
+        s = np.float32(m / np.float32(127.0))
+        if not (s >= np.float32(2.0 ** -126)):
+            continue
+        k = rng.integers(-127, 127, 100000).astype(np.float64) + 0.5
+        g = (k * np.float64(s)).astype(np.float32)
+        steps = rng.integers(-4, 5, g.size)
+        for step in range(1, 5):
+            g = np.where(steps >= step, np.nextafter(g, np.float32(np.inf)), g)
+            g = np.where(steps <= -step, np.nextafter(g, np.float32(-np.inf)), g)
+        g = np.clip(g, -m, m)
+        q, _ = kernel_codes(g, s)
+        assert np.array_equal(q, reference_codes(g, s)), trial
+
+
+def test_fast_path_power_of_two_scales_exact_ties():
+    for e in range(-126, 120, 7):
+        s = np.float32(2.0 ** e)
+        k = np.arange(-127, 127, dtype=np.float64) + 0.5
+        g = (k * 2.0 ** e).astype(np.float32)
+        q, near = kernel_codes(g, s)
+        assert np.all(near)  # every exact tie goes to the division
+        assert np.array_equal(q, reference_codes(g, s))
+
+
+def _level_tree(terms):
+    level = list(terms)
+    while len(level) > 1:
+        nxt = ["(%s+%s)" % (level[p], level[p + 1]) for p in range(0, len(level) - 1, 2)]
+        if len(level) % 2:
+            nxt.append(level[-1])
+        level = nxt
+    return level[0]
+
+
+def _counter_tree(terms):
+    st, count = {}, 0
+    for x in terms:
+        c, k = count, 0
+        while c & 1:
+            x = "(%s+%s)" % (st[k], x)
+            k += 1
+            c >>= 1
+        st[k] = x
+        count += 1
+    acc = None
+    for b in range(8):
+        if count & (1 << b):
+            acc = st[b] if acc is None else "(%s+%s)" % (st[b], acc)
+    return acc
+
+
+def test_counter_tree_pairs_like_level_tree():
+    for W in range(1, 65):
+        terms = ["d%d" % r for r in range(W)]
+        assert _counter_tree(terms) == _level_tree(terms), W
+
+
+def test_absmax_before_unscale():
+    rng = np.random.default_rng(2)
+    for inv in [np.float32(2.0 ** -16), np.float32(1.0 / 3.0), np.float32(1.0 / 1000.0), np.float32(7.0)]:
+        x = (rng.standard_normal(100000) * 10.0 ** rng.uniform(-40, 30, 100000)).astype(np.float32)
+        x = x[np.isfinite(x)]
+        g = x * inv
+        assert np.float32(np.abs(g).max()) == np.float32(np.abs(x).max() * inv)

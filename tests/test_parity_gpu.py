@@ -1,0 +1,341 @@
+"""GPU path against the oracle, through the C ABI, element by element.
+
+Codes, scales, the chunk table and the sequential / ring sums are compared bit for bit;
+the tree order too (the kernel uses the same pairing as the oracle) and, separately, to
+|tree - seq| <= 1e-6 * sum |terms|.  Every output buffer carries guard canaries."""
+import numpy as np
+import pytest
+import torch
+
+import dp_gradient_bucket_gb300 as gq
+import oracle
+import workloads as wl
+import _gpu as H
+
+pytestmark = pytest.mark.gpu
+
+ORDERS = [("seq", oracle.SEQ), ("ring", oracle.RING), ("tree", oracle.TREE)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+
+
+def _rows(cfg, W, n):
+    return wl.rows(cfg, W, n)
+
+
+# ------------------------------------------------------------------ workload 1 (small, full)
+
+@pytest.mark.parametrize("order,oorder", ORDERS)
+@pytest.mark.parametrize("mode", ["fused", "two_kernel"])
+def test_workload1_full(order, oorder, mode):
+    W, n = 2, 262144
+    host, stride = _rows(1, W, n)
+    out, codes, scales, off, st = H.run(host, W, stride, [n], order, mode=mode)
+    assert st == gq.GQ_OK
+    assert np.array_equal(off, oracle.plan_chunks([n], 4))
+    H.compare_full(host, W, stride, off, oorder, 1.0, out, codes, scales)
+
+
+# ------------------------------------------------------------------ workload 2 (headline, full)
+
+@pytest.mark.parametrize("order,oorder", ORDERS)
+def test_workload2_full_fused(order, oorder):
+    W, n = 8, 6553600
+    host, stride = _rows(2, W, n)
+    out, codes, scales, off, st = H.run(host, W, stride, [n], order)
+    assert st == gq.GQ_OK and len(off) == 201
+    H.compare_full(host, W, stride, off, oorder, 1.0, out, codes, scales)
+
+
+def test_workload2_two_kernel_ring():
+    W, n = 8, 6553600
+    host, stride = _rows(2, W, n)
+    out, codes, scales, off, st = H.run(host, W, stride, [n], "ring", mode="two_kernel")
+    assert st == gq.GQ_OK
+    H.compare_full(host, W, stride, off, oracle.RING, 1.0, out, codes, scales)
+
+
+def test_workload2_without_codes_output_is_deterministic():
+    """The timed configuration (no codes / scales written), three runs: identical bits."""
+    W, n = 8, 6553600
+    host, stride = _rows(2, W, n)
+    want = oracle.fused(host, W, stride, oracle.plan_chunks([n], 4), oracle.RING)[0]
+    for _ in range(3):
+        out, _, _, _, st = H.run(host, W, stride, [n], "ring", want_codes=False)
+        assert st == gq.GQ_OK
+        H.assert_bits_equal(out, want, "output")
+
+
+def test_tree_within_tolerance_of_seq():
+    W, n = 8, 6553600
+    host, stride = _rows(2, W, n)
+    tree, codes, scales, off, _ = H.run(host, W, stride, [n], "tree")
+    seq = oracle.reduce(codes, scales, W, stride, off, oracle.SEQ)
+    chunk = np.repeat(np.arange(len(off) - 1), np.diff(off))
+    terms = np.zeros(n)
+    for r in range(W):
+        terms += np.abs(codes[r * stride:r * stride + n].astype(np.float64) * scales[r, chunk])
+    assert np.all(np.abs(tree.astype(np.float64) - seq) <= 1e-6 * terms / W + 1e-45)
+
+
+# ------------------------------------------------------------------ workload 3 (ResNet-152 list)
+
+def test_workload3_buckets_and_full_ring():
+    W = 8
+    sizes, _ = wl.tensor_layout(3)
+    n = int(sizes.sum())
+    bot, buckets = gq.gq_plan_buckets(sizes, 4)
+    obot, obuckets = oracle.assign_buckets(sizes, 4)
+    assert list(buckets) == list(obuckets) and list(bot) == list(obot)
+    host, stride = _rows(3, W, n)
+    out, codes, scales, off, st = H.run(host, W, stride, list(buckets), "ring")
+    assert st == gq.GQ_OK
+    assert np.array_equal(off, oracle.plan_chunks(buckets, 4))
+    H.compare_full(host, W, stride, off, oracle.RING, 1.0, out, codes, scales)
+
+
+def test_workload3_seq_sampled():
+    W = 8
+    sizes, _ = wl.tensor_layout(3)
+    n = int(sizes.sum())
+    _, buckets = gq.gq_plan_buckets(sizes, 4)
+    host, stride = _rows(3, W, n)
+    out, codes, scales, off, st = H.run(host, W, stride, list(buckets), "seq")
+    assert st == gq.GQ_OK
+    rows2d = host.reshape(W, stride)
+    H.compare_sampled(lambda lo, hi: rows2d[:, lo:hi], W, off, H.sample_chunks(len(off) - 1, 60, 3),
+                      oracle.SEQ, 1.0, out, codes, scales, stride)
+
+
+# ------------------------------------------------------------------ workload 4 (BERT-Large fp16)
+
+def test_workload4_bert_fp16_sampled():
+    W = 16
+    dev = torch.device("cuda:0")
+    sizes, _ = wl.tensor_layout(4)
+    n = int(sizes.sum())
+    assert n == 335141888
+    _, buckets = gq.gq_plan_buckets(sizes, 2)
+    stride = gq.row_stride(n, 2)
+    grads = torch.empty(W * stride, dtype=torch.float16, device=dev)
+    tmp = np.zeros(stride, dtype=np.float16)
+    for r in range(W):  # one rank at a time: 670 MB of host memory, not 10.7 GB
+        wl.fill(4, r, 0, n, tmp[:n])
+        grads[r * stride:(r + 1) * stride].copy_(torch.from_numpy(tmp))
+    nc, d_off = H.plan_device(list(buckets), 2, dev)
+    off = d_off.cpu().numpy()
+    assert np.array_equal(off, oracle.plan_chunks(buckets, 2))
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    scales = torch.empty(W * nc, dtype=torch.float32, device=dev)
+    gq.gq_fused_allreduce_sim(grads, W, stride, d_off, nc, 65536.0, "ring", out, None, scales)
+    assert gq.gq_get_error() == gq.GQ_OK
+    out_h = out.cpu().numpy()
+    scales_h = scales.cpu().numpy().reshape(W, nc)
+    del grads
+
+    def rows(lo, hi):
+        return np.stack([wl.fill(4, r, lo, hi) for r in range(W)])
+
+    # bucket boundaries, first / last / random chunks
+    starts = np.concatenate([[0], np.cumsum(buckets)[:-1]])
+    bucket_first = [int(np.searchsorted(off, s)) for s in starts]
+    chunks = sorted(set(H.sample_chunks(nc, 40, 4)) | set(bucket_first))
+    H.compare_sampled(rows, W, off, chunks, oracle.RING, 65536.0, out_h, None, scales_h, stride)
+
+
+def test_fp16_unscale_full_small():
+    """fp16 with loss scales 65536 (exact unscale) and 3 (inexact), both orders, full compare."""
+    W, n = 16, 300007
+    sizes = np.array([n])
+    host = np.zeros(W * gq.row_stride(n, 2), dtype=np.float16)
+    stride = gq.row_stride(n, 2)
+    for r in range(W):
+        wl.fill(4, r, 0, n, host[r * stride:r * stride + n])
+    for ls in (65536.0, 3.0):
+        for order, oorder in ORDERS[:2]:
+            for mode in ("fused", "two_kernel"):
+                out, codes, scales, off, st = H.run(host, W, stride, [n], order, loss_scale=ls, mode=mode)
+                assert st == gq.GQ_OK
+                H.compare_full(host, W, stride, off, oorder, ls, out, codes, scales)
+
+
+# ------------------------------------------------------------------ workload 5 (size sweep)
+
+SMALL_SWEEP = [s for s in wl.SWEEP_SIZES if s <= 1 << 22]
+LARGE_SWEEP = [s for s in wl.SWEEP_SIZES if s > 1 << 22]
+
+
+def _sweep_rows(W, n):
+    host, stride = wl.rows(5, W, n)
+    off = oracle.plan_chunks([n], 4)
+    if len(off) - 1 >= 5:
+        wl.adversarial(host, W, stride, off)
+    return host, stride, off
+
+
+@pytest.mark.parametrize("n", SMALL_SWEEP)
+def test_workload5_sweep_full(n):
+    W = 8
+    host, stride, off = _sweep_rows(W, n)
+    for order, oorder in ORDERS[:2]:
+        out, codes, scales, doff, st = H.run(host, W, stride, [n], order)
+        assert st == gq.GQ_OK
+        assert np.array_equal(doff, off)
+        H.compare_full(host, W, stride, off, oorder, 1.0, out, codes, scales)
+    out, codes, scales, _, st = H.run(host, W, stride, [n], "ring", mode="two_kernel")
+    H.compare_full(host, W, stride, off, oracle.RING, 1.0, out, codes, scales)
+
+
+@pytest.mark.parametrize("n", LARGE_SWEEP)
+def test_workload5_sweep_sampled(n):
+    W = 8
+    host, stride, off = _sweep_rows(W, n)
+    out, codes, scales, doff, st = H.run(host, W, stride, [n], "ring")
+    assert st == gq.GQ_OK
+    assert np.array_equal(doff, off)
+    rows2d = host.reshape(W, stride)
+    chunks = sorted(set(range(min(6, len(off) - 1))) | set(H.sample_chunks(len(off) - 1, 24, n % 997)))
+    H.compare_sampled(lambda lo, hi: rows2d[:, lo:hi], W, off, chunks, oracle.RING, 1.0, out, codes, scales,
+                      stride)
+    # properties at any size: |q| <= 127 for normal scales, the code range, and the mean bound
+    chunk = np.repeat(np.arange(len(off) - 1), np.diff(off))
+    normal = scales >= np.float32(2.0 ** -126)
+    c2 = codes.reshape(W, stride)[:, :n]
+    assert np.all(np.abs(c2[normal[:, chunk]].astype(np.int32)) <= 127)
+
+
+# ------------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("W", [1, 3, 5, 16, 33, 64])
+def test_rank_counts(W):
+    n = 100003
+    host = np.zeros(W * gq.row_stride(n, 4), dtype=np.float32)
+    stride = gq.row_stride(n, 4)
+    for r in range(W):
+        wl.fill(1, r, 0, n, host[r * stride:r * stride + n])
+    for order, oorder in ORDERS:
+        for mode in ("fused", "two_kernel"):
+            out, codes, scales, off, st = H.run(host, W, stride, [n], order, mode=mode)
+            assert st == gq.GQ_OK
+            H.compare_full(host, W, stride, off, oorder, 1.0, out, codes, scales)
+
+
+def test_multi_bucket_ragged_table():
+    """Buckets of odd sizes (chunks start off the 16-byte grid), an empty bucket in the
+    middle, tiny buckets shorter than W, and a 256 KiB-minus-4-bytes single chunk that
+    exceeds the staging rows (the re-read path)."""
+    W = 8
+    buckets = [5, 0, 1, 65535, 131075, 7, 32769 * 3 + 1, 3]
+    n = sum(buckets)
+    host = np.zeros(W * gq.row_stride(n, 4), dtype=np.float32)
+    stride = gq.row_stride(n, 4)
+    for r in range(W):
+        wl.fill(2, r, 0, n, host[r * stride:r * stride + n])
+    for order, oorder in ORDERS:
+        for mode in ("fused", "two_kernel"):
+            out, codes, scales, off, st = H.run(host, W, stride, buckets, order, mode=mode)
+            assert st == gq.GQ_OK
+            assert np.array_equal(off, oracle.plan_chunks(buckets, 4))
+            H.compare_full(host, W, stride, off, oorder, 1.0, out, codes, scales)
+
+
+def test_empty_bucket_only():
+    W = 4
+    host = np.zeros(W * 4, dtype=np.float32)
+    out, codes, scales, off, st = H.run(host, W, 4, [0], "ring")
+    assert st == gq.GQ_OK
+    assert list(off) == [0, 0]
+    assert np.all(scales == 0)
+
+
+def test_constant_ranks_self_test():
+    """Rank r holds r + 1 everywhere: every code 127 and the mean (W+1)/2 within 4 ulp,
+    bit-equal to the oracle (the ones*rank all_reduce self-test pattern)."""
+    W, n = 8, 70000
+    stride = gq.row_stride(n, 4)
+    host = np.zeros(W * stride, dtype=np.float32)
+    for r in range(W):
+        host[r * stride:r * stride + n] = r + 1
+    out, codes, scales, off, st = H.run(host, W, stride, [n], "ring")
+    assert st == gq.GQ_OK
+    assert np.all(codes.reshape(W, stride)[:, :n] == 127)
+    assert np.all(np.abs(out[:n] - 4.5) <= 4 * np.spacing(np.float32(4.5)))
+    H.compare_full(host, W, stride, off, oracle.RING, 1.0, out, codes, scales)
+
+
+def test_nonfinite_input_is_reported():
+    W, n = 4, 300000
+    stride = gq.row_stride(n, 4)
+    host = np.zeros(W * stride, dtype=np.float32)
+    for r in range(W):
+        wl.fill(1, r, 0, n, host[r * stride:r * stride + n])
+    host[1 * stride + 5] = np.inf      # chunk 0 of rank 1
+    host[3 * stride + 200000] = np.nan  # a later chunk of rank 3
+    off = oracle.plan_chunks([n], 4)
+    for mode in ("fused", "two_kernel"):
+        out, codes, scales, _, st = H.run(host, W, stride, [n], "ring", mode=mode)
+        assert st == gq.GQ_WARN_NONFINITE
+        want, _, wscales, nf = oracle.fused(host, W, stride, off, oracle.RING)
+        assert nf == 2
+        bad = {0, int(np.searchsorted(off, 200000, side="right") - 1)}
+        for j in range(len(off) - 1):
+            if j in bad:
+                continue
+            lo, hi = off[j], off[j + 1]
+            H.assert_bits_equal(out[lo:hi], want[lo:hi], "finite chunk %d" % j)
+    assert gq.gq_get_error() == gq.GQ_OK  # the word was cleared by the read
+
+
+def _rebased(host, W, stride, lo, hi, order):
+    n = hi - lo
+    s2 = gq.row_stride(n, 4)
+    rows = np.zeros(W * s2, dtype=np.float32)
+    for r in range(W):
+        rows[r * s2:r * s2 + n] = host[r * stride + lo:r * stride + hi]
+    return oracle.fused(rows, W, s2, np.array([0, n]), order)[0]
+
+
+def test_bad_chunk_table_is_reported_and_skipped():
+    """Table entries past the row end or negative make their chunks invalid: those are
+    skipped and reported; the valid chunks (which do not overlap) are still computed.
+    Every index stays inside the buffers (the kernels check a chunk before touching it)."""
+    W, n = 4, 4096
+    stride = gq.row_stride(n, 4)
+    host = np.zeros(W * stride, dtype=np.float32)
+    for r in range(W):
+        wl.fill(1, r, 0, n, host[r * stride:r * stride + n])
+    # chunks: [0,1000) ok, [1000,5000) past the row, [5000,2000) backwards, [2000,3000) ok,
+    #         [3000,-5) backwards, [-5,100) negative start
+    table = np.array([0, 1000, 5000, 2000, 3000, -5, 100], dtype=np.int64)
+    for mode in ("fused", "two_kernel"):
+        for order, oorder in ORDERS:
+            out, codes, scales, _, st = H.run(host, W, stride, None, order, mode=mode, offsets=table)
+            assert st == gq.GQ_ERR_BAD_TABLE
+            H.assert_bits_equal(out[0:1000], _rebased(host, W, stride, 0, 1000, oorder), "chunk 0")
+            H.assert_bits_equal(out[2000:3000], _rebased(host, W, stride, 2000, 3000, oorder), "chunk 3")
+            untouched = np.concatenate([out[1000:2000], out[3000:]]).view(np.uint32)
+            assert np.all(untouched == H.CANARY_F32)
+
+
+def test_non_default_stream_and_fp32_loss_scale():
+    W, n = 8, 500001
+    stride = gq.row_stride(n, 4)
+    host = np.zeros(W * stride, dtype=np.float32)
+    for r in range(W):
+        wl.fill(2, r, 0, n, host[r * stride:r * stride + n])
+    s = torch.cuda.Stream()
+    dev = torch.device("cuda:0")
+    with torch.cuda.stream(s):
+        grads = torch.from_numpy(host).to(dev)
+        nc, d_off = H.plan_device([n], 4, dev, stream=s)
+        out = torch.empty(n, dtype=torch.float32, device=dev)
+        gq.gq_fused_allreduce_sim(grads, W, stride, d_off, nc, 1024.0, "ring", out, stream=s)
+        assert gq.gq_get_error(s) == gq.GQ_OK
+    want = oracle.fused(host, W, stride, oracle.plan_chunks([n], 4), oracle.RING, 1024.0)[0]
+    H.assert_bits_equal(out.cpu().numpy(), want, "output")
