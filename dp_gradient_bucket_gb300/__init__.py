@@ -51,6 +51,8 @@ def _load():
     L.gq_reduce_dequant.argtypes = [p, p, i32, sz, p, sz, i32, p, p]
     L.gq_fused_allreduce_sim.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p]
     L.gq_get_error.argtypes = [p]
+    L.gq_testing_inject_copy_stall.argtypes = [ctypes.c_uint32, ctypes.c_uint64]
+    L.gq_testing_inject_copy_stall.restype = i32
     L.gq_status_string.argtypes = [i32]
     L.gq_status_string.restype = ctypes.c_char_p
     for name in ("gq_plan_buckets", "gq_plan_chunks", "gq_quantize", "gq_reduce_dequant",
@@ -160,3 +162,9 @@ def row_stride(n, elem_bytes):
     """Smallest rank_stride >= n (and >= 1 group) whose rows start on 16-byte boundaries."""
     per = 16 // elem_bytes
     return max(per, -(-int(n) // per) * per)
+
+
+def gq_testing_inject_copy_stall(extra_bytes, limit_ns):
+    """Fault injection (include/gq_testing.h): the fused kernel's bulk-copy wait expects
+    extra_bytes more than arrive and gives up after limit_ns; (0, 0) restores the defaults."""
+    _check(lib.gq_testing_inject_copy_stall(int(extra_bytes), int(limit_ns)), "gq_testing_inject_copy_stall")

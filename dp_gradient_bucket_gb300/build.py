@@ -44,7 +44,8 @@ def _stale(target, deps):
 
 
 def build(force=False, verbose_ptxas=False):
-    deps = [os.path.join(CSRC, s) for s in SOURCES + HEADERS] + [os.path.join(ROOT, "include", "gq.h")]
+    deps = [os.path.join(CSRC, s) for s in SOURCES + HEADERS] + [
+        os.path.join(ROOT, "include", h) for h in ("gq.h", "gq_testing.h")]
     if not force and not _stale(LIB, deps):
         return LIB
     os.makedirs(BUILD, exist_ok=True)

@@ -7,6 +7,7 @@
 #include <vector>
 
 #include "../../include/gq.h"
+#include "../../include/gq_testing.h"
 #include "gq_internal.h"
 
 namespace {
@@ -212,6 +213,11 @@ gq_status gq_get_error(gq_stream_t stream) {
     if (w & gq::kErrBadTable) return GQ_ERR_BAD_TABLE;
     if (w & gq::kErrNonfinite) return GQ_WARN_NONFINITE;
     return GQ_OK;
+}
+
+gq_status gq_testing_inject_copy_stall(uint32_t extra_bytes, uint64_t limit_ns) {
+    if (extra_bytes == 0 && limit_ns == 0) limit_ns = 2000000000ull;
+    return gq::set_copy_stall(extra_bytes, limit_ns) == cudaSuccess ? GQ_OK : GQ_ERR_CUDA;
 }
 
 const char* gq_status_string(gq_status s) {

@@ -48,6 +48,10 @@ cudaError_t launch_reduce(const int8_t* codes, const float* scales, int W, int64
 cudaError_t launch_fused(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales,
                          cudaStream_t stream);
 
+// Fault injection for tests: extra expected bytes on the fused kernel's bulk-copy barrier and
+// the wait limit (synchronous, current device).
+cudaError_t set_copy_stall(uint32_t extra_bytes, uint64_t limit_ns);
+
 // Reads and clears the current device's error word (synchronous).
 cudaError_t read_and_clear_error_word(unsigned* word, cudaStream_t stream);
 

@@ -25,13 +25,21 @@ __device__ unsigned g_error_word;
 __device__ __forceinline__ void raise_error(unsigned bit) { atomicOr(&g_error_word, bit); }
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s for a bulk copy that takes microseconds
+
+// Bulk-copy wait settings; changed only by the fault-injection hook of the tests.
+__device__ uint64_t g_wait_limit_ns = kWaitLimitNs;
+__device__ uint32_t g_stall_extra_tx = 0;
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ bool chunk_bounds(const int64_t* offsets, int64_t j, int64_t rank_stride,
-                                             int64_t* lo, int64_t* hi) {
+// Chunk j is used only if 0 <= lo <= hi <= min(rank_stride, offsets[num_chunks]): then every
+// row access stays inside its row and every output index inside out[0, offsets[num_chunks]),
+// whatever the rest of the table holds.
+__device__ __forceinline__ bool chunk_bounds(const int64_t* offsets, int64_t j, int64_t num_chunks,
+                                             int64_t rank_stride, int64_t* lo, int64_t* hi) {
     *lo = __ldg(offsets + j);
     *hi = __ldg(offsets + j + 1);
-    return *lo >= 0 && *lo <= *hi && *hi <= rank_stride && (*hi - *lo) <= INT_MAX;
+    const int64_t end = __ldg(offsets + num_chunks);
+    return *lo >= 0 && *lo <= *hi && *hi <= rank_stride && *hi <= end && (*hi - *lo) <= INT_MAX;
 }
 
 __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* scratch) {
@@ -114,7 +122,7 @@ __global__ void __launch_bounds__(kThreads) k_quantize(const QuantArgs a, int8_t
     const int64_t j = blockIdx.x;
     const int r = blockIdx.y;
     int64_t lo, hi;
-    if (!chunk_bounds(a.offsets, j, a.rank_stride, &lo, &hi)) {
+    if (!chunk_bounds(a.offsets, j, a.num_chunks, a.rank_stride, &lo, &hi)) {
         if (threadIdx.x == 0 && r == 0) raise_error(kErrBadTable);
         return;
     }
@@ -202,7 +210,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const int8_t* codes, const 
     __shared__ float s_scale[kMaxRanks];
     const int64_t j = blockIdx.x;
     int64_t lo, hi;
-    if (!chunk_bounds(offsets, j, rank_stride, &lo, &hi)) {
+    if (!chunk_bounds(offsets, j, num_chunks, rank_stride, &lo, &hi)) {
         if (threadIdx.x == 0 && blockIdx.y == 0) raise_error(kErrBadTable);
         return;
     }
@@ -329,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const FusedArgs A) {
     int64_t lo, hi;
     // The table entry is the same for every CTA of the cluster, so a bad chunk makes the
     // whole cluster leave here, before any cluster barrier.
-    if (!chunk_bounds(A.q.offsets, j, A.q.rank_stride, &lo, &hi)) {
+    if (!chunk_bounds(A.q.offsets, j, A.q.num_chunks, A.q.rank_stride, &lo, &hi)) {
         if (tid == 0 && crank == 0) raise_error(kErrBadTable);
         return;
     }
@@ -349,15 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const FusedArgs A) {
         fence_barrier_init();
     }
     __syncthreads();
+    const uint64_t wait_limit = g_wait_limit_ns;
     if (staged && tid == 0) {
-        mbar_arrive_expect_tx(&bar, slice_bytes * static_cast<uint32_t>(W));
+        mbar_arrive_expect_tx(&bar, slice_bytes * static_cast<uint32_t>(W) + g_stall_extra_tx);
         for (int r = 0; r < W; ++r)
             bulk_copy_g2s(stage + static_cast<uint32_t>(r) * A.row_cap, grads + r * row_bytes + sg0 * 16, slice_bytes,
                           &bar);
     }
     bool copied = true;
     if (staged) {
-        copied = mbar_wait_bounded(&bar, 0, kWaitLimitNs);
+        copied = mbar_wait_bounded(&bar, 0, wait_limit);
         if (!copied) raise_error(kErrTimeout);
     }
     auto load_group = [&](int r, int64_t g) -> V16 {
@@ -501,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_fused(const FusedArgs A) {
     }
 
     cluster_wait_acquire();  // no CTA leaves while a peer may still read its partial maxima
-    if (staged && !copied) mbar_wait_bounded(&bar, 0, kWaitLimitNs);  // let late copies land
+    if (staged && !copied) mbar_wait_bounded(&bar, 0, wait_limit);  // let late copies land
 }
 
 // Per-rank staging capacity for a cluster of P: chunks up to 144 KiB per rank (dynamic_chunk
@@ -608,6 +617,12 @@ cudaError_t launch_fused(const QuantArgs& a, int order, float* out, int8_t* code
 }
 
 // ===================================================================== error word
+
+cudaError_t set_copy_stall(uint32_t extra_bytes, uint64_t limit_ns) {
+    cudaError_t e = cudaMemcpyToSymbol(g_stall_extra_tx, &extra_bytes, sizeof(extra_bytes));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_wait_limit_ns, &limit_ns, sizeof(limit_ns));
+}
 
 cudaError_t read_and_clear_error_word(unsigned* word, cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);

@@ -23,7 +23,8 @@ def gq():
 
 
 def _declared():
-    src = open(os.path.join(ROOT, "include", "gq.h")).read()
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(gq_[a-z_]+)\s*\(", src)))
 

@@ -302,25 +302,28 @@ def _rebased(host, W, stride, lo, hi, order):
 
 
 def test_bad_chunk_table_is_reported_and_skipped():
-    """Table entries past the row end or negative make their chunks invalid: those are
-    skipped and reported; the valid chunks (which do not overlap) are still computed.
-    Every index stays inside the buffers (the kernels check a chunk before touching it)."""
+    """Entries past the row end, past the table's last entry, backwards or negative make
+    their chunks invalid: those are skipped and reported, and the valid chunks (which do not
+    overlap) are still computed.  Every index stays inside the buffers: a chunk is used only
+    if 0 <= lo <= hi <= min(rank_stride, offsets[num_chunks])."""
     W, n = 4, 4096
     stride = gq.row_stride(n, 4)
     host = np.zeros(W * stride, dtype=np.float32)
     for r in range(W):
         wl.fill(1, r, 0, n, host[r * stride:r * stride + n])
     # chunks: [0,1000) ok, [1000,5000) past the row, [5000,2000) backwards, [2000,3000) ok,
-    #         [3000,-5) backwards, [-5,100) negative start
-    table = np.array([0, 1000, 5000, 2000, 3000, -5, 100], dtype=np.int64)
+    #         [3000,9000) past the row, [9000,-5) backwards, [-5,3500) negative, [3500,3600) ok
+    table = np.array([0, 1000, 5000, 2000, 3000, 9000, -5, 3500, 3600], dtype=np.int64)
+    good = [(0, 1000), (2000, 3000), (3500, 3600)]
     for mode in ("fused", "two_kernel"):
         for order, oorder in ORDERS:
             out, codes, scales, _, st = H.run(host, W, stride, None, order, mode=mode, offsets=table)
             assert st == gq.GQ_ERR_BAD_TABLE
-            H.assert_bits_equal(out[0:1000], _rebased(host, W, stride, 0, 1000, oorder), "chunk 0")
-            H.assert_bits_equal(out[2000:3000], _rebased(host, W, stride, 2000, 3000, oorder), "chunk 3")
-            untouched = np.concatenate([out[1000:2000], out[3000:]]).view(np.uint32)
-            assert np.all(untouched == H.CANARY_F32)
+            written = np.zeros(len(out), dtype=bool)
+            for lo, hi in good:
+                H.assert_bits_equal(out[lo:hi], _rebased(host, W, stride, lo, hi, oorder), "chunk %d" % lo)
+                written[lo:hi] = True
+            assert np.all(out[~written].view(np.uint32) == H.CANARY_F32)
 
 
 def test_non_default_stream_and_fp32_loss_scale():
