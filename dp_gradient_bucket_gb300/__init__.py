@@ -5,7 +5,8 @@ PyTorch is used for device memory and streams.  There is no fallback: if libgq.s
 missing or fails to load, importing the binding raises.
 
 Functions keep the C names: gq_plan_buckets, gq_plan_chunks, gq_quantize,
-gq_reduce_dequant, gq_fused_allreduce_sim, gq_get_error, gq_status_string.  Device
+gq_reduce_dequant, gq_fused_allreduce_sim, gq_fused_workspace_bytes, gq_fused_allreduce_sim_ws,
+gq_get_error, gq_status_string.  Device
 arguments are CUDA torch tensors (contiguous; their storage is used as is); `stream` is a
 torch.cuda.Stream, a raw cudaStream_t integer, or None for torch's current stream.
 """
@@ -50,13 +51,16 @@ def _load():
     L.gq_quantize.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, p, p, p]
     L.gq_reduce_dequant.argtypes = [p, p, i32, sz, p, sz, i32, p, p]
     L.gq_fused_allreduce_sim.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p]
+    L.gq_fused_allreduce_sim_ws.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p, sz, p]
+    L.gq_fused_workspace_bytes.argtypes = [sz, i32]
+    L.gq_fused_workspace_bytes.restype = sz
     L.gq_get_error.argtypes = [p]
     L.gq_testing_inject_copy_stall.argtypes = [ctypes.c_uint32, ctypes.c_uint64]
     L.gq_testing_inject_copy_stall.restype = i32
     L.gq_status_string.argtypes = [i32]
     L.gq_status_string.restype = ctypes.c_char_p
     for name in ("gq_plan_buckets", "gq_plan_chunks", "gq_quantize", "gq_reduce_dequant",
-                 "gq_fused_allreduce_sim", "gq_get_error"):
+                 "gq_fused_allreduce_sim", "gq_fused_allreduce_sim_ws", "gq_get_error"):
         getattr(L, name).restype = i32
     return L
 
@@ -151,6 +155,21 @@ def gq_fused_allreduce_sim(grads, W, rank_stride, d_offsets, num_chunks, loss_sc
                                     num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out),
                                     _dptr(codes), _dptr(scales), _stream(stream))
     _check(st, "gq_fused_allreduce_sim")
+
+
+def gq_fused_workspace_bytes(num_chunks, W):
+    return lib.gq_fused_workspace_bytes(int(num_chunks), int(W))
+
+
+def gq_fused_allreduce_sim_ws(grads, W, rank_stride, d_offsets, num_chunks, loss_scale, order, out, workspace,
+                              codes=None, scales=None, stream=None):
+    """gq_fused_allreduce_sim with a device workspace (a zero-filled CUDA tensor of at least
+    gq_fused_workspace_bytes(num_chunks, W) bytes, left zero-filled by every successful call)."""
+    st = lib.gq_fused_allreduce_sim_ws(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
+                                       num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out), _dptr(codes),
+                                       _dptr(scales), _dptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream))
+    _check(st, "gq_fused_allreduce_sim_ws")
 
 
 def gq_get_error(stream=None):

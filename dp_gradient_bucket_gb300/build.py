@@ -15,8 +15,9 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libgq.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["gq_kernels.cu", "gq_api.cu"]
-HEADERS = ["gq_device.cuh", "gq_internal.h"]
+SOURCES = ["gq_reg_f16.cu", "gq_reg_f32.cu", "gq_queue_f16.cu", "gq_queue_f32.cu", "gq_fused_f16.cu", "gq_fused_f32.cu",
+           "gq_kernels.cu", "gq_api.cu"]
+HEADERS = ["gq_device.cuh", "gq_internal.h", "gq_fused.cuh", "gq_queue.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-Wall", "-I" + os.path.join(ROOT, "include")]
@@ -43,16 +44,20 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force=False, verbose_ptxas=False):
+def build(force=False, verbose_ptxas=False, extra_flags=(), out=None):
+    """Compile and link libgq.so (to `out`, default in the package directory).  extra_flags
+    go to every nvcc compile (e.g. -D settings of the kernels' launch bounds)."""
+    lib = out or LIB
+    build_dir = os.path.join(os.path.dirname(lib), "_build") if out else BUILD
     deps = [os.path.join(CSRC, s) for s in SOURCES + HEADERS] + [
         os.path.join(ROOT, "include", h) for h in ("gq.h", "gq_testing.h")]
-    if not force and not _stale(LIB, deps):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if not force and not _stale(lib, deps):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
+    extra = (["-Xptxas", "-v"] if verbose_ptxas else []) + list(extra_flags)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src + ".o")
+        obj = os.path.join(build_dir, src + ".o")
         cmd = [nvcc()] + NVCC_FLAGS + extra + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -62,17 +67,17 @@ def build(force=False, verbose_ptxas=False):
     with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
         results = list(ex.map(compile_one, SOURCES))
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     libdir = cuda_lib_dir()
     cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs + [
         "-L" + libdir, "-Xlinker", "-rpath=" + libdir]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose_ptxas:
-        return LIB, "\n".join(err for _, err in results)
-    return LIB
+        return lib, "\n".join(err for _, err in results)
+    return lib
 
 
 if __name__ == "__main__":

@@ -6,8 +6,8 @@
 #include <cstdint>
 #include <vector>
 
-#include "../../include/gq.h"
-#include "../../include/gq_testing.h"
+#include "gq.h"
+#include "gq_testing.h"
 #include "gq_internal.h"
 
 namespace {
@@ -203,6 +203,36 @@ gq_status gq_fused_allreduce_sim(const void* d_grads, gq_dtype dt, int W, size_t
     const gq::QuantArgs a = quant_args(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
     return from_cuda(gq::launch_fused(a, static_cast<int>(order), d_out, d_codes_opt, d_scales_opt,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t gq_fused_workspace_bytes(size_t num_chunks, int W) {
+    if (W < 1) W = 1;
+    return 4 * (2 + num_chunks * (static_cast<size_t>(W) + 1));
+}
+
+gq_status gq_fused_allreduce_sim_ws(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                    const int64_t* d_offsets, size_t num_chunks, float loss_scale, gq_order order,
+                                    float* d_out, int8_t* d_codes_opt, float* d_scales_opt, void* d_workspace,
+                                    size_t workspace_bytes, gq_stream_t stream) {
+    gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
+    if (st != GQ_OK) return st;
+    if (!d_out || !d_workspace) return GQ_ERR_INVALID_ARG;
+    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (workspace_bytes < gq_fused_workspace_bytes(num_chunks, W)) return GQ_ERR_INVALID_ARG;
+    if (!aligned(d_out, 16) || !aligned(d_workspace, 16) || (d_codes_opt && !aligned(d_codes_opt, 16)) ||
+        (d_scales_opt && !aligned(d_scales_opt, 4)))
+        return GQ_ERR_MISALIGNED;
+    const size_t gbytes = static_cast<size_t>(W) * rank_stride * elem_bytes_of(dt);
+    const size_t obytes = rank_stride * 4, cbytes = d_codes_opt ? static_cast<size_t>(W) * rank_stride : 0,
+                 sbytes = d_scales_opt ? static_cast<size_t>(W) * num_chunks * 4 : 0;
+    const void* bufs[5] = {d_grads, d_out, d_codes_opt, d_scales_opt, d_workspace};
+    const size_t sizes[5] = {gbytes, obytes, cbytes, sbytes, workspace_bytes};
+    for (int x = 0; x < 5; ++x)
+        for (int y = x + 1; y < 5; ++y)
+            if (overlaps(bufs[x], sizes[x], bufs[y], sizes[y])) return GQ_ERR_INVALID_ARG;
+    const gq::QuantArgs a = quant_args(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
+    return from_cuda(gq::launch_fused_ws(a, static_cast<int>(order), d_out, d_codes_opt, d_scales_opt,
+                                         static_cast<uint32_t*>(d_workspace), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gq_status gq_get_error(gq_stream_t stream) {

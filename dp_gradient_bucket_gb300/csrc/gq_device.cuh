@@ -34,14 +34,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// One try_wait: the warp may be suspended in hardware for up to ~65 us while the phase is
+// incomplete, so a waiting CTA issues almost no instructions.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(65536u)
         : "memory");
     return done != 0;
 }
@@ -72,6 +74,30 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
         : "memory");
 }
 
+// L2 cache policies for bulk copies (createpolicy): keep lines that will be read again soon,
+// or let lines read for the last time go first.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// bulk_copy_g2s with an L2 cache policy.
+__device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                   uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- thread-block clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -86,6 +112,14 @@ __device__ __forceinline__ void cluster_arrive_release() {
 
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Atomic max into the same shared-memory variable in CTA `cta` of this cluster (fire and
+// forget; ordered before a later barrier.cluster.arrive.release).
+__device__ __forceinline__ void dsmem_red_max_u32(const void* local, uint32_t cta, uint32_t v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(cta));
+    asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
 
 // Load a u32 from the same shared-memory variable in CTA `cta` of this cluster.
@@ -147,6 +181,45 @@ template <>
 __device__ __forceinline__ uint32_t group_abs_bits<1>(const V16& v, int e) {
     const uint32_t w = v.w[e >> 1];
     return ((e & 1) ? (w >> 16) : w) & 0x7fffu;
+}
+
+// ---------------------------------------------------------------- packed fp32 pairs (sm_100+)
+// add / sub / mul on two binary32 lanes in one instruction; each lane is an IEEE operation with
+// round-to-nearest-even, subnormals kept, never contracted into an FMA.
+
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 sub2_rn(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// max(m, |x|) with NaN propagated (a NaN anywhere leaves a NaN, whose bit pattern then orders
+// above +Inf), so the running absmax still flags non-finite chunks.
+__device__ __forceinline__ float absmax_acc(float m, float x) {
+    float r;
+    asm("{\n\t.reg .f32 t;\n\tabs.f32 t, %2;\n\tmax.NaN.f32 %0, %1, t;\n\t}" : "=f"(r) : "f"(m), "f"(x));
+    return r;
 }
 
 // ---------------------------------------------------------------- quantiser arithmetic

@@ -146,6 +146,28 @@ gq_status gq_fused_allreduce_sim(const void* d_grads, gq_dtype dt, int W, size_t
                                  gq_order order, float* d_out, int8_t* d_codes_opt,
                                  float* d_scales_opt, gq_stream_t stream);
 
+/* Bytes of device workspace gq_fused_allreduce_sim_ws needs for a chunk table of num_chunks chunks
+ * and W ranks (4 * (2 + num_chunks * (W + 1))). */
+size_t gq_fused_workspace_bytes(size_t num_chunks, int W);
+
+/* gq_fused_allreduce_sim with a caller-owned device workspace: same arguments, same results bit for
+ * bit.  For W = 8 it runs the pass over HBM as a work queue that needs no thread-block clusters:
+ * per-slice absmax items stream the gradients from HBM, and per-slice reduce items read them back
+ * from L2 once their chunk's absmax is settled (a small wait on a per-chunk count, bounded in time).
+ * For other W it runs the kernel of gq_fused_allreduce_sim and leaves the workspace alone.
+ *   d_workspace      device memory of at least gq_fused_workspace_bytes(num_chunks, W) bytes,
+ *                    16-byte aligned, ZERO-FILLED before its first use (one cudaMemset after
+ *                    allocation).  A call that completes normally leaves it zero-filled again, so it
+ *                    can be reused call after call; after a call that reported GQ_ERR_TIMEOUT or
+ *                    GQ_ERR_BAD_TABLE it must be zero-filled again.  Calls that share a workspace
+ *                    must not overlap on the device (use one stream, or one workspace per stream).
+ *   workspace_bytes  its size; GQ_ERR_INVALID_ARG if it is short. */
+gq_status gq_fused_allreduce_sim_ws(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                    const int64_t* d_offsets, size_t num_chunks, float loss_scale,
+                                    gq_order order, float* d_out, int8_t* d_codes_opt,
+                                    float* d_scales_opt, void* d_workspace, size_t workspace_bytes,
+                                    gq_stream_t stream);
+
 /* Waits for `stream`, then reads and clears the current device's error word.  Returns
  * GQ_OK, or the most serious recorded condition: GQ_ERR_TIMEOUT, then GQ_ERR_BAD_TABLE,
  * then GQ_WARN_NONFINITE; GQ_ERR_CUDA if the wait or the read failed. */

@@ -55,13 +55,21 @@ def run(host_rows, W, stride, bucket_elems, order, loss_scale=1.0, mode="fused",
     codes_buf = i8_canary(W * stride, dev)
     scales_buf = f32_canary(W * nc, dev)
     out, codes, scales = inner(out_buf, n_out), inner(codes_buf, W * stride), inner(scales_buf, W * nc)
+    ws = None
     if mode == "fused":
         gq.gq_fused_allreduce_sim(grads, W, stride, d_off, nc, loss_scale, order, out,
                                   codes if want_codes else None, scales if want_codes else None)
+    elif mode == "fused_ws":
+        ws = torch.zeros(gq.gq_fused_workspace_bytes(nc, W) // 4, dtype=torch.int32, device=dev)
+        for _ in range(2):  # a second call on the same workspace: it must have been left zeroed
+            gq.gq_fused_allreduce_sim_ws(grads, W, stride, d_off, nc, loss_scale, order, out, ws,
+                                         codes if want_codes else None, scales if want_codes else None)
     else:
         gq.gq_quantize(grads, W, stride, d_off, nc, loss_scale, codes, scales)
         gq.gq_reduce_dequant(codes, scales, W, stride, d_off, nc, order, out)
     status = gq.gq_get_error()
+    if ws is not None and status == gq.GQ_OK:
+        assert int(ws.abs().sum().item()) == 0, "workspace not left zero-filled"
     assert guards_intact(out_buf, n_out), "write outside the output buffer"
     assert guards_intact(codes_buf, W * stride), "write outside the codes buffer"
     assert guards_intact(scales_buf, W * nc), "write outside the scales buffer"

@@ -15,7 +15,9 @@ pytestmark = pytest.mark.gpu
 
 
 def test_bulk_copy_wait_runs_out_and_is_reported():
-    W, n = 8, 262144           # 8 chunks of 32,768: the shared-memory staged path
+    # W = 4 runs the cluster kernel that stages each slice in shared memory with bulk copies (the
+    # W = 8 register-staged kernel has no bulk-copy wait); 8 chunks of 32,768
+    W, n = 4, 262144
     host, stride = wl.rows(2, W, n)
     off = oracle.plan_chunks([n], 4)
     assert gq.gq_get_error() == gq.GQ_OK

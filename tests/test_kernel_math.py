@@ -27,6 +27,20 @@ def kernel_codes(g, s):
     return (u - M).astype(np.int64), near
 
 
+def kernel_codes_scaled(x, inv, s):
+    """The mode-1 decision with the unscale folded in: t = x * fl(inv * rcp(s)); the exact
+    fallback unscales g = fl(x * inv) and divides."""
+    x = x.astype(np.float32)
+    c = inv * (np.float32(1.0) / s)
+    t = x * c
+    u = t + M
+    d = t - (u - M)
+    near = np.abs(d) > NEAR_TIE
+    y = (x * inv) / s
+    u = np.where(near, y + M, u)
+    return (u - M).astype(np.int64), near
+
+
 def reference_codes(g, s):
     y = g.astype(np.float32) / s
     return np.clip(np.rint(y), -128, 127).astype(np.int64)
@@ -76,6 +90,42 @@ def test_fast_path_power_of_two_scales_exact_ties():
         q, near = kernel_codes(g, s)
         assert np.all(near)  # every exact tie goes to the division
         assert np.array_equal(q, reference_codes(g, s))
+
+
+def test_folded_unscale_matches_exact_division():
+    """fp16 gradients with loss scales 65536, 1024, 3, 1000 (inexact inverses): the folded
+    constant c = fl(inv * rcp(s)) keeps t within 2^-15 of g / s, inside the 2^-14 band."""
+    rng = np.random.default_rng(3)
+    for ls in (65536.0, 1024.0, 3.0, 1000.0, 7.5):
+        inv = np.float32(1.0 / ls)
+        for trial in range(60):
+            bits = rng.integers(0, 0x7c00, 200000).astype(np.uint16)
+            h = bits.view(np.float16).astype(np.float32) * np.where(rng.random(200000) < 0.5, -1, 1).astype(np.float32)
+            g = h * inv
+            m = np.abs(g).max()
+            s = np.float32(m / np.float32(127.0))
+            if not (s >= np.float32(2.0 ** -126)):
+                continue
+            q, _ = kernel_codes_scaled(h, inv, s)
+            assert np.array_equal(q, reference_codes(g, s)), (ls, trial)
+        # values placed at the near-tie band of the quotient
+        for trial in range(40):
+            m = np.float32(10.0 ** rng.uniform(-3, 4))
+            s = np.float32(m / np.float32(127.0))
+            k = rng.integers(-127, 127, 100000).astype(np.float64) + 0.5
+            g = (k * np.float64(s)).astype(np.float32)
+            h = (g.astype(np.float64) * ls).astype(np.float32)
+            for step in (1, 2, 3):
+                h = np.where(rng.random(h.size) < 0.3, np.nextafter(h, np.float32(np.inf)), h)
+                h = np.where(rng.random(h.size) < 0.3, np.nextafter(h, np.float32(-np.inf)), h)
+            g = h * inv
+            g = np.clip(g, -m, m)
+            h = np.where(np.abs(h * inv) > m, (g.astype(np.float64) * ls).astype(np.float32), h)
+            g = h * inv
+            mm = np.abs(g).max()
+            s = np.float32(mm / np.float32(127.0))
+            q, _ = kernel_codes_scaled(h, inv, s)
+            assert np.array_equal(q, reference_codes(g, s)), (ls, trial)
 
 
 def _level_tree(terms):

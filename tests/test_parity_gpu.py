@@ -45,10 +45,11 @@ def test_workload1_full(order, oorder, mode):
 # ------------------------------------------------------------------ workload 2 (headline, full)
 
 @pytest.mark.parametrize("order,oorder", ORDERS)
-def test_workload2_full_fused(order, oorder):
+@pytest.mark.parametrize("mode", ["fused", "fused_ws"])
+def test_workload2_full_fused(order, oorder, mode):
     W, n = 8, 6553600
     host, stride = _rows(2, W, n)
-    out, codes, scales, off, st = H.run(host, W, stride, [n], order)
+    out, codes, scales, off, st = H.run(host, W, stride, [n], order, mode=mode)
     assert st == gq.GQ_OK and len(off) == 201
     H.compare_full(host, W, stride, off, oorder, 1.0, out, codes, scales)
 
@@ -61,13 +62,14 @@ def test_workload2_two_kernel_ring():
     H.compare_full(host, W, stride, off, oracle.RING, 1.0, out, codes, scales)
 
 
-def test_workload2_without_codes_output_is_deterministic():
+@pytest.mark.parametrize("mode", ["fused", "fused_ws"])
+def test_workload2_without_codes_output_is_deterministic(mode):
     """The timed configuration (no codes / scales written), three runs: identical bits."""
     W, n = 8, 6553600
     host, stride = _rows(2, W, n)
     want = oracle.fused(host, W, stride, oracle.plan_chunks([n], 4), oracle.RING)[0]
     for _ in range(3):
-        out, _, _, _, st = H.run(host, W, stride, [n], "ring", want_codes=False)
+        out, _, _, _, st = H.run(host, W, stride, [n], "ring", want_codes=False, mode=mode)
         assert st == gq.GQ_OK
         H.assert_bits_equal(out, want, "output")
 
@@ -86,7 +88,8 @@ def test_tree_within_tolerance_of_seq():
 
 # ------------------------------------------------------------------ workload 3 (ResNet-152 list)
 
-def test_workload3_buckets_and_full_ring():
+@pytest.mark.parametrize("mode", ["fused", "fused_ws"])
+def test_workload3_buckets_and_full_ring(mode):
     W = 8
     sizes, _ = wl.tensor_layout(3)
     n = int(sizes.sum())
@@ -94,7 +97,7 @@ def test_workload3_buckets_and_full_ring():
     obot, obuckets = oracle.assign_buckets(sizes, 4)
     assert list(buckets) == list(obuckets) and list(bot) == list(obot)
     host, stride = _rows(3, W, n)
-    out, codes, scales, off, st = H.run(host, W, stride, list(buckets), "ring")
+    out, codes, scales, off, st = H.run(host, W, stride, list(buckets), "ring", mode=mode)
     assert st == gq.GQ_OK
     assert np.array_equal(off, oracle.plan_chunks(buckets, 4))
     H.compare_full(host, W, stride, off, oracle.RING, 1.0, out, codes, scales)
@@ -184,10 +187,11 @@ def test_workload5_sweep_full(n):
     W = 8
     host, stride, off = _sweep_rows(W, n)
     for order, oorder in ORDERS[:2]:
-        out, codes, scales, doff, st = H.run(host, W, stride, [n], order)
-        assert st == gq.GQ_OK
-        assert np.array_equal(doff, off)
-        H.compare_full(host, W, stride, off, oorder, 1.0, out, codes, scales)
+        for mode in ("fused", "fused_ws"):
+            out, codes, scales, doff, st = H.run(host, W, stride, [n], order, mode=mode)
+            assert st == gq.GQ_OK
+            assert np.array_equal(doff, off)
+            H.compare_full(host, W, stride, off, oorder, 1.0, out, codes, scales)
     out, codes, scales, _, st = H.run(host, W, stride, [n], "ring", mode="two_kernel")
     H.compare_full(host, W, stride, off, oracle.RING, 1.0, out, codes, scales)
 
@@ -238,7 +242,7 @@ def test_multi_bucket_ragged_table():
     for r in range(W):
         wl.fill(2, r, 0, n, host[r * stride:r * stride + n])
     for order, oorder in ORDERS:
-        for mode in ("fused", "two_kernel"):
+        for mode in ("fused", "fused_ws", "two_kernel"):
             out, codes, scales, off, st = H.run(host, W, stride, buckets, order, mode=mode)
             assert st == gq.GQ_OK
             assert np.array_equal(off, oracle.plan_chunks(buckets, 4))
@@ -262,7 +266,7 @@ def test_constant_ranks_self_test():
     host = np.zeros(W * stride, dtype=np.float32)
     for r in range(W):
         host[r * stride:r * stride + n] = r + 1
-    out, codes, scales, off, st = H.run(host, W, stride, [n], "ring")
+    out, codes, scales, off, st = H.run(host, W, stride, [n], "ring", mode="fused_ws")
     assert st == gq.GQ_OK
     assert np.all(codes.reshape(W, stride)[:, :n] == 127)
     assert np.all(np.abs(out[:n] - 4.5) <= 4 * np.spacing(np.float32(4.5)))
@@ -306,7 +310,7 @@ def test_bad_chunk_table_is_reported_and_skipped():
     their chunks invalid: those are skipped and reported, and the valid chunks (which do not
     overlap) are still computed.  Every index stays inside the buffers: a chunk is used only
     if 0 <= lo <= hi <= min(rank_stride, offsets[num_chunks])."""
-    W, n = 4, 4096
+    W, n = 8, 4096
     stride = gq.row_stride(n, 4)
     host = np.zeros(W * stride, dtype=np.float32)
     for r in range(W):
@@ -315,7 +319,7 @@ def test_bad_chunk_table_is_reported_and_skipped():
     #         [3000,9000) past the row, [9000,-5) backwards, [-5,3500) negative, [3500,3600) ok
     table = np.array([0, 1000, 5000, 2000, 3000, 9000, -5, 3500, 3600], dtype=np.int64)
     good = [(0, 1000), (2000, 3000), (3500, 3600)]
-    for mode in ("fused", "two_kernel"):
+    for mode in ("fused", "two_kernel", "fused_ws"):
         for order, oorder in ORDERS:
             out, codes, scales, _, st = H.run(host, W, stride, None, order, mode=mode, offsets=table)
             assert st == gq.GQ_ERR_BAD_TABLE
