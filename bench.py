@@ -4,7 +4,7 @@ Workload: W = 8 virtual ranks, one flat 25 MiB fp32 DDP bucket (6,553,600 elemen
 rank, Laplace(0, 1e-4) values with 30% exact zeros and 0.1% outliers x100, dynamic_chunk
 into 200 chunks of 32,768, ring-order int8 dequantise-sum, mean.  A step is one pass of the
 whole path: the chunk table (gq_plan_chunks) and the fused quantise + reduce
-(gq_fused_allreduce_sim) over one input set.  Steps rotate over input sets whose total is
+(gq_fused_allreduce_sim, or gq_fused_allreduce_sim_ws with --entry ws) over one input set.  Steps rotate over input sets whose total is
 several times the 129 MB L2, so every step reads its gradients from HBM.
 
 Metric: input GB/s = W * n * 4 bytes per step / step time (the fused kernel also writes
@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length (cpu_baseline)")
+    p.add_argument("--entry", default="plain", choices=["ws", "plain"],
+                   help="ws: gq_fused_allreduce_sim_ws (work-queue kernel); plain: gq_fused_allreduce_sim")
     return p.parse_args()
 
 
@@ -229,10 +231,18 @@ def run_gq(args):
     offsets = torch.empty(nc + 1, dtype=torch.int64, device=dev)
     out = torch.empty(N_ELEMS, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # the caller-owned workspace of the work-queue entry point: zeroed once, left zeroed by every call
+    wspace = torch.zeros(gq.gq_fused_workspace_bytes(nc, W) // 4, dtype=torch.int32, device=dev)
+
+    def fused(inp):
+        if args.entry == "ws":
+            gq.gq_fused_allreduce_sim_ws(inp, W, stride, offsets, nc, 1.0, "ring", out, wspace, stream=stream)
+        else:
+            gq.gq_fused_allreduce_sim(inp, W, stride, offsets, nc, 1.0, "ring", out, stream=stream)
 
     def step(k):
         gq.gq_plan_chunks([N_ELEMS], eb, offsets, stream)
-        gq.gq_fused_allreduce_sim(sets[k % INPUT_SETS], W, stride, offsets, nc, 1.0, "ring", out, stream=stream)
+        fused(sets[k % INPUT_SETS])
 
     for k in range(max(args.warmup, 3)):
         step(k)
@@ -254,7 +264,7 @@ def run_gq(args):
     for k in range(args.steps):
         gq.gq_plan_chunks([N_ELEMS], eb, offsets, stream)
         ev_start[k].record(stream)
-        gq.gq_fused_allreduce_sim(sets[k % INPUT_SETS], W, stride, offsets, nc, 1.0, "ring", out, stream=stream)
+        fused(sets[k % INPUT_SETS])
         ev_end[k].record(stream)
     t_all1.record(stream)
     torch.cuda.synchronize()
@@ -281,7 +291,7 @@ def run_gq(args):
     for _ in range(2):
         dev_in.copy_(pinned_in, non_blocking=True)
         gq.gq_plan_chunks([N_ELEMS], eb, offsets, stream)
-        gq.gq_fused_allreduce_sim(dev_in, W, stride, offsets, nc, 1.0, "ring", out, stream=stream)
+        fused(dev_in)
         pinned_out.copy_(out, non_blocking=True)
     barrier(ws)
     torch.cuda.synchronize()
@@ -290,7 +300,7 @@ def run_gq(args):
     for _ in range(e2e_steps):
         dev_in.copy_(pinned_in, non_blocking=True)
         gq.gq_plan_chunks([N_ELEMS], eb, offsets, stream)
-        gq.gq_fused_allreduce_sim(dev_in, W, stride, offsets, nc, 1.0, "ring", out, stream=stream)
+        fused(dev_in)
         pinned_out.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -308,15 +318,16 @@ def run_gq(args):
     peak = float(peaks["hbm_gbs"])
     alg_bytes = IN_BYTES + OUT_BYTES
     achieved = alg_bytes / (kern_avg_ms * 1e-3) / 1e9
+    kernel = "k_queue<f32>" if args.entry == "ws" else "k_fused<f32, W=8>"
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "fused_traffic.json")
     if os.path.exists(tpath):
         try:
             with open(tpath) as f:
-                tj = json.load(f)
+                tj = json.load(f).get(kernel, {})
             if tj.get("kernel_source_hash") == kernel_source_hash():
                 traffic = tj.get("dram_bytes_per_launch")
-        except (OSError, ValueError):
+        except (OSError, ValueError, AttributeError):
             traffic = None
 
     import oracle  # cpu_baseline leg only
@@ -329,10 +340,11 @@ def run_gq(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "order": "ring", "chunks": nc, "input_bytes_per_step": IN_BYTES,
                    "l2": "%d rotating input sets of %d MB (> 129 MB L2)" % (INPUT_SETS, IN_BYTES // 10 ** 6),
-                   "step": "gq_plan_chunks + gq_fused_allreduce_sim"},
+                   "step": "gq_plan_chunks + " + ("gq_fused_allreduce_sim_ws" if args.entry == "ws"
+                                                  else "gq_fused_allreduce_sim")},
         "hbm_peak_fraction": value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "kernel": "k_fused<f32>", "kernel_avg_us": kern_avg_ms * 1e3,
+                     "traffic": traffic, "kernel": kernel, "kernel_avg_us": kern_avg_ms * 1e3,
                      "algorithmic_bytes_per_launch": alg_bytes, "peak_source": peak_kind},
         "cpu_baseline": {"value": cpu_gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": "%d full passes of the workload (8 x 6,553,600 fp32, ring) in %.1f s" % (
@@ -349,11 +361,15 @@ def run_gq(args):
 
 
 def kernel_source_hash():
+    """Hash of the device sources the timed kernels are built from (traffic figures taken from an
+    ncu capture count only while it matches)."""
     import hashlib
     h = hashlib.sha256()
-    for f in ("gq_kernels.cu", "gq_device.cuh"):
-        with open(os.path.join(ROOT, "dp_gradient_bucket_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    csrc = os.path.join(ROOT, "dp_gradient_bucket_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 

@@ -163,8 +163,9 @@ def gq_fused_workspace_bytes(num_chunks, W):
 
 def gq_fused_allreduce_sim_ws(grads, W, rank_stride, d_offsets, num_chunks, loss_scale, order, out, workspace,
                               codes=None, scales=None, stream=None):
-    """gq_fused_allreduce_sim with a device workspace (a zero-filled CUDA tensor of at least
-    gq_fused_workspace_bytes(num_chunks, W) bytes, left zero-filled by every successful call)."""
+    """gq_fused_allreduce_sim with a device workspace: a CUDA tensor of at least
+    gq_fused_workspace_bytes(num_chunks, W) bytes, zero-filled before its first use and then passed
+    unchanged from call to call (zero it again only after a GQ_ERR_TIMEOUT)."""
     st = lib.gq_fused_allreduce_sim_ws(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
                                        num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out), _dptr(codes),
                                        _dptr(scales), _dptr(workspace), workspace.numel() * workspace.element_size(),

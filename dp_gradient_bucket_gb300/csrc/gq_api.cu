@@ -207,7 +207,7 @@ gq_status gq_fused_allreduce_sim(const void* d_grads, gq_dtype dt, int W, size_t
 
 size_t gq_fused_workspace_bytes(size_t num_chunks, int W) {
     if (W < 1) W = 1;
-    return 4 * (2 + num_chunks * (static_cast<size_t>(W) + 1));
+    return 16 + num_chunks * 32 * static_cast<size_t>(W) * 8;
 }
 
 gq_status gq_fused_allreduce_sim_ws(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
@@ -232,7 +232,8 @@ gq_status gq_fused_allreduce_sim_ws(const void* d_grads, gq_dtype dt, int W, siz
             if (overlaps(bufs[x], sizes[x], bufs[y], sizes[y])) return GQ_ERR_INVALID_ARG;
     const gq::QuantArgs a = quant_args(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
     return from_cuda(gq::launch_fused_ws(a, static_cast<int>(order), d_out, d_codes_opt, d_scales_opt,
-                                         static_cast<uint32_t*>(d_workspace), reinterpret_cast<cudaStream_t>(stream)));
+                                         static_cast<uint32_t*>(d_workspace), workspace_bytes,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 gq_status gq_get_error(gq_stream_t stream) {

@@ -9,12 +9,11 @@
 // unscale before quantising; mean over the group as in the "torchtitan-npu 3D parallel"
 // article (framerc.cn/news/2545645), AMP + 3D section.
 //
-// Two kernels, one chunk per thread-block cluster, CTA p of the cluster owning slice p:
-//   k_fused_pipe (W = 8)  persistent: each chunk's slice is bulk-copied into shared memory, moved
-//                into registers, and the next chunk's copy starts while the current one is
-//                exchanged, quantised and summed; the gradients cross HBM exactly once;
-//   k_fused      (any W)  the slice is bulk-copied into shared memory (TMA) when it fits, else
-//                read twice from global memory (the second time from L2).
+// k_fused: one chunk per thread-block cluster, CTA p of the cluster owning slice p.  For W other
+// than 8 the slice is bulk-copied into shared memory (TMA) when it fits; for W = 8 (compiled for
+// that W), and for slices that do not fit, it is read twice from global memory, the second time
+// from L2: on GB300 the re-read form ran the 25 MiB W = 8 bucket in 92 us against 164 us staged,
+// its CTAs being small enough for three to share an SM.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -217,56 +216,6 @@ __device__ __forceinline__ void fast_group(Load load, int W, const RowScales& rs
     store_out<VEC>(A.out, e0, full, slo, shi, o);
 }
 
-// The fast path for fp32 groups in the sequential / ring order.  The quantiser steps run on packed
-// pairs: t = x * c, u = t + M, n = u - M, d = t - n take one instruction per two element-ranks.
-// Those steps need no fixed rounding sequence to be exact: were any of them fused, t and d would only
-// move closer to x * c, which lies within 2^-15 of g / s, and every integer decision still falls
-// outside the 2^-14 near-tie band or into the exact fallback.  The dequantise-and-sum steps
-// dq = n * s, acc + dq, whose two roundings the result depends on, stay scalar __fmul_rn /
-// __fadd_rn, which are never contracted.  Same values, bit for bit, as fast_group.
-template <int WC, bool CODES, class Load>
-__device__ __forceinline__ void fast_group_f32x2(Load load, int W, const RowScales& rs, int64_t e0, bool full,
-                                                 int64_t slo, int64_t shi, const Args& A, bool pow2) {
-#ifdef GQ_NO_F32X2
-    fast_group<0, WC, CODES, false>(load, W, rs, e0, full, slo, shi, A, pow2);
-    return;
-#endif
-    const float2 M2 = make_float2(kMagic, kMagic);
-    float acc[4];
-    bool near = false;
-    const int KW = WC ? WC : W;
-#pragma unroll
-    for (int k = 0; k < KW; ++k) {
-        const V16 v = load(k);
-        const float c = rs.c[k], s = rs.s[k];
-        const float2 c2 = make_float2(c, c);
-        const float2 x0 = make_float2(__uint_as_float(v.w[0]), __uint_as_float(v.w[1]));
-        const float2 x1 = make_float2(__uint_as_float(v.w[2]), __uint_as_float(v.w[3]));
-        const float2 t0 = mul2_rn(x0, c2), t1 = mul2_rn(x1, c2);
-        const float2 u0 = add2_rn(t0, M2), u1 = add2_rn(t1, M2);
-        const float2 n0 = sub2_rn(u0, M2), n1 = sub2_rn(u1, M2);
-        const float2 d0 = sub2_rn(t0, n0), d1 = sub2_rn(t1, n1);
-        near |= (fabsf(d0.x) > kNearTie) | (fabsf(d0.y) > kNearTie) | (fabsf(d1.x) > kNearTie) |
-                (fabsf(d1.y) > kNearTie);
-        const float q[4] = {__fmul_rn(n0.x, s), __fmul_rn(n0.y, s), __fmul_rn(n1.x, s), __fmul_rn(n1.y, s)};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] = k == 0 ? q[e] : __fadd_rn(acc[e], q[e]);
-        if (CODES && A.codes) {
-            const uint32_t packed[1] = {code_byte(u0.x) | (code_byte(u0.y) << 8) | (code_byte(u1.x) << 16) |
-                                        (code_byte(u1.y) << 24)};
-            store_codes<4>(A.codes + static_cast<int64_t>(rs.rank[k]) * A.q.rank_stride, e0, full, slo, shi, packed);
-        }
-    }
-    if (near) {  // rare: the exact division decides every element-rank of the group
-        fast_group<0, WC, CODES, false>(load, W, rs, e0, full, slo, shi, A, pow2);
-        return;
-    }
-    float o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[e] = mean_of(acc[e], W, A.invW, pow2);
-    store_out<4>(A.out, e0, full, slo, shi, o);
-}
-
 // General path for one group: any scale (subnormal scales divide and clamp everywhere), and a
 // ring group that spans two segments (each element gets its own start rank).
 // load_rank(r) returns the group of rank r.
@@ -414,7 +363,7 @@ __device__ __forceinline__ bool exchange_scales(const Args& A, int W, uint32_t P
 }
 
 #ifndef GQ_FUSED_MIN_CTAS_F32
-#define GQ_FUSED_MIN_CTAS_F32 2
+#define GQ_FUSED_MIN_CTAS_F32 3
 #endif
 #ifndef GQ_FUSED_MIN_CTAS_F16
 #define GQ_FUSED_MIN_CTAS_F16 1
@@ -542,8 +491,6 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? GQ_FUSED_MIN_CTAS_F32 : GQ
             auto ld = [&](int k) { return load_row(k, g); };
             if (A.order == kOrderTree)
                 fast_group<DT, WC, CODES, true>(ld, W, rs, e0, full, sl.lo, sl.hi, A, pow2);
-            else if (DT == 0)
-                fast_group_f32x2<WC, CODES>(ld, W, rs, e0, full, sl.lo, sl.hi, A, pow2);
             else
                 fast_group<DT, WC, CODES, false>(ld, W, rs, e0, full, sl.lo, sl.hi, A, pow2);
         } else {
@@ -552,259 +499,6 @@ __global__ void __launch_bounds__(kThreads, DT == 0 ? GQ_FUSED_MIN_CTAS_F32 : GQ
         }
     }
     if (staged && !copied) mbar_wait_bounded(&bar, 0, wait_limit);  // let late copies land
-}
-
-// ----------------------------------------------------------------------------- k_fused_pipe
-// Persistent, register-staged form for W known at compile time (8).  The grid holds as many
-// clusters of P CTAs as fit at once; cluster c takes chunks c, c + G, c + 2G, ...  Per chunk:
-//   1. wait for the CTA's slice in the shared-memory stage (cp.async.bulk, one copy per rank row,
-//      row k holding rank (k + rot) % W), and copy it into registers (kPipeGroups 16-byte groups
-//      of every row per thread);
-//   2. the stage is free again: one thread issues the bulk copies of the next chunk's slice, which
-//      stream in while the rest of this chunk is processed;
-//   3. absmax from the registers, pushed to every peer CTA with remote atomic max; one cluster
-//      barrier per chunk (partials double-buffered by chunk parity);
-//   4. scales, then quantise, dequantise, sum over rows and store from the same registers.
-// The gradients cross HBM once and the copy of the next chunk overlaps the exchange, the
-// arithmetic and the stores of the current one.  Slices too large for the stage or the register
-// tile are read from global memory (twice for the groups past the register tile).
-constexpr int kPipeThreads = 256;
-constexpr int kPipeGroups = 2;
-
-struct PipeGeom {
-    bool valid;
-    int64_t lo, hi;
-    uint32_t seg;
-    Slice sl;
-    int rot;
-    bool uniform;
-    uint32_t bytes;  // per rank row
-    bool staged;
-};
-
-template <int VEC>
-__device__ __forceinline__ PipeGeom pipe_geom(const Args& A, int W, int64_t j, uint32_t crank) {
-    PipeGeom g;
-    g.valid = chunk_bounds(A.q.offsets, j, A.q.num_chunks, A.q.rank_stride, &g.lo, &g.hi);
-    g.seg = g.valid && g.hi > g.lo ? static_cast<uint32_t>((g.hi - g.lo + W - 1) / W) : 1u;
-    g.sl = cta_slice<VEC>(A, W, g.valid ? g.lo : 0, g.valid ? g.hi : 0, g.seg, crank);
-    g.uniform = true;
-    g.rot = 0;
-    if (g.valid && A.order == kOrderRing && g.sl.hi > g.sl.lo) {
-        const int t0 = segment_of(g.sl.lo, g.lo, g.seg), t1 = segment_of(g.sl.hi - 1, g.lo, g.seg);
-        g.uniform = t0 == t1;
-        if (g.uniform) g.rot = (t0 + 1 == W) ? 0 : t0 + 1;
-    }
-    g.bytes = static_cast<uint32_t>((g.sl.g1 - g.sl.g0) * 16);
-    g.staged = g.valid && g.sl.g1 > g.sl.g0 && A.row_cap != 0 && g.bytes <= A.row_cap;
-    return g;
-}
-
-template <int DT, int WC, bool CODES>
-__global__ void __launch_bounds__(kPipeThreads, 2) k_fused_pipe(const Args A) {
-    constexpr int VEC = DT == 0 ? 4 : 8;
-    constexpr int EB = DT == 0 ? 4 : 2;
-    constexpr int W = WC;
-    constexpr int NWARP = kPipeThreads / 32;
-    extern __shared__ __align__(128) unsigned char stage[];
-    __shared__ uint64_t bar;
-    __shared__ uint32_t part[2][W];        // chunk absmax by rank, double-buffered by chunk parity
-    __shared__ uint32_t wmax[NWARP][W];    // per-warp partials of the row-k rank
-    __shared__ ScaleQ sq[W];
-    __shared__ float row_s[W], row_c[W];
-    __shared__ int row_rank[W];
-    __shared__ int s_stop;                 // a copy wait ran out: stop staging, read global memory
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t P = A.P;
-    const uint32_t crank = cluster_ctarank();
-    const int64_t cid = blockIdx.x / P, G = gridDim.x / P;
-    const int64_t nchunks = cid < A.q.num_chunks ? (A.q.num_chunks - cid + G - 1) / G : 0;
-    const char* grads = static_cast<const char*>(A.q.grads);
-    const int64_t row_bytes = A.q.rank_stride * EB;
-    const uint64_t wait_limit = g_wait_limit_ns;
-    const bool pow2 = (W & (W - 1)) == 0;
-    const bool tree = A.order == kOrderTree;
-
-    if (tid < W) part[0][tid] = part[1][tid] = 0;
-    if (tid == 0) {
-        s_stop = 0;
-        mbar_init(&bar, 1);
-        fence_barrier_init();
-    }
-    __syncthreads();
-    cluster_arrive_release();  // every CTA's part[] is zero before any peer pushes into it
-    cluster_wait_acquire();
-
-    // thread 0 only: bulk copies of a chunk's slice, row k <- rank (k + rot) % W
-    auto issue = [&](const PipeGeom& g) {
-        mbar_arrive_expect_tx(&bar, g.bytes * static_cast<uint32_t>(W) + g_stall_extra_tx);
-#pragma unroll
-        for (int k = 0; k < W; ++k)
-            bulk_copy_g2s(stage + static_cast<uint32_t>(k) * A.row_cap,
-                          grads + static_cast<int64_t>((k + g.rot) % W) * row_bytes + g.sl.g0 * 16, g.bytes, &bar);
-    };
-    uint32_t phase = 0;   // uses of `bar` waited for (thread 0's view: issued copies)
-    bool pending = false; // thread 0: a copy was issued and not yet waited for
-    if (tid == 0 && nchunks > 0) {
-        const PipeGeom g0 = pipe_geom<VEC>(A, W, cid, crank);
-        if (g0.staged) {
-            issue(g0);
-            pending = true;
-        }
-    }
-
-    for (int64_t i = 0; i < nchunks; ++i) {
-        const int64_t j = cid + i * G;
-        const PipeGeom g = pipe_geom<VEC>(A, W, j, crank);
-        const bool staged_now = g.staged && ld_volatile_shared_int(&s_stop) == 0;
-        V16 v[kPipeGroups][W];
-        if (g.valid) {
-            if (staged_now) {
-                const bool ok = mbar_wait_bounded(&bar, phase & 1u, wait_limit);
-                if (!ok) {
-                    if (tid == 0) {
-                        raise_error(kErrTimeout);
-                        st_volatile_shared_int(&s_stop, 1);
-                    }
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < kPipeGroups; ++q) {
-                const int64_t gi = g.sl.g0 + tid + q * kPipeThreads;
-                if (gi < g.sl.g1) {
-#pragma unroll
-                    for (int k = 0; k < W; ++k)
-                        v[q][k] = staged_now
-                                      ? ld_shared_v16(stage + static_cast<uint32_t>(k) * A.row_cap + (gi - g.sl.g0) * 16)
-                                      : ld_global_nc_v16(grads + static_cast<int64_t>((k + g.rot) % W) * row_bytes + gi * 16);
-                }
-            }
-        }
-        if (staged_now) ++phase;
-        __syncthreads();  // the stage has been read into registers, and the last chunk finished, by every thread
-        if (tid < W) row_rank[tid] = (tid + g.rot) % W;
-
-        // ---- the next chunk's slice streams in while this one is finished
-        if (tid == 0) {
-            // re-arm the barrier only after the previous use completed (never twice in a phase)
-            const bool prev_done = !pending || mbar_try_wait(&bar, (phase - 1u) & 1u);
-            pending = false;
-            if (i + 1 < nchunks && s_stop == 0) {  // the table is read only for chunks that exist
-                const PipeGeom gn = pipe_geom<VEC>(A, W, j + G, crank);
-                if (gn.staged) {
-                    if (prev_done) {
-                        issue(gn);
-                        pending = true;
-                    } else {
-                        raise_error(kErrTimeout);
-                        s_stop = 1;
-                    }
-                }
-            }
-        }
-
-        if (g.valid) {
-            // ---- absmax per rank from registers
-            uint32_t mx[W];
-#pragma unroll
-            for (int k = 0; k < W; ++k) mx[k] = 0;
-#pragma unroll
-            for (int q = 0; q < kPipeGroups; ++q) {
-                const int64_t gi = g.sl.g0 + tid + q * kPipeThreads;
-                if (gi < g.sl.g1) {
-                    const int64_t e0 = gi * VEC;
-                    const bool full = e0 >= g.sl.lo && e0 + VEC <= g.sl.hi;
-#pragma unroll
-                    for (int k = 0; k < W; ++k) mx[k] = group_absmax<DT>(v[q][k], e0, full, g.sl.lo, g.sl.hi, mx[k]);
-                }
-            }
-            for (int64_t gi = g.sl.g0 + tid + kPipeGroups * kPipeThreads; gi < g.sl.g1; gi += kPipeThreads) {
-                const int64_t e0 = gi * VEC;
-                const bool full = e0 >= g.sl.lo && e0 + VEC <= g.sl.hi;
-#pragma unroll
-                for (int k = 0; k < W; ++k)
-                    mx[k] = group_absmax<DT>(ld_global_nc_v16(grads + static_cast<int64_t>((k + g.rot) % W) * row_bytes + gi * 16),
-                                             e0, full, g.sl.lo, g.sl.hi, mx[k]);
-            }
-#pragma unroll
-            for (int k = 0; k < W; ++k) {
-                const uint32_t m = __reduce_max_sync(0xffffffffu, mx[k]);
-                if (lane == 0) wmax[warp][k] = m;
-            }
-            __syncthreads();
-            // ---- this CTA's partials into every peer's part[parity]
-            for (int t = tid; t < W * static_cast<int>(P); t += kPipeThreads) {
-                const int k = t % W;
-                uint32_t m = 0;
-#pragma unroll
-                for (int w = 0; w < NWARP; ++w) m = max(m, wmax[w][k]);
-                if (m != 0) dsmem_red_max_u32(&part[i & 1][(k + g.rot) % W], static_cast<uint32_t>(t / W), m);
-            }
-            cluster_arrive_release();
-            cluster_wait_acquire();  // part[parity][r] of every CTA is the chunk's max for rank r
-
-            // ---- scales (part[parity] zeroed again for the chunk after next)
-            const float inv = A.q.inv;
-            const bool scaled = A.q.scaled != 0;
-            bool not_subnormal = true;
-            if (tid < W) {
-                const uint32_t mraw = part[i & 1][tid];
-                part[i & 1][tid] = 0;
-                float m = DT == 0 ? __uint_as_float(mraw)
-                                  : __half2float(__ushort_as_half(static_cast<unsigned short>(mraw)));
-                if (scaled) m = __fmul_rn(m, inv);
-                const bool nonfinite = (DT == 0 ? mraw >= 0x7f800000u : mraw >= 0x7c00u) || !(fabsf(m) <= 3.40282347e38f);
-                const ScaleQ s = make_scale(m);
-                sq[tid] = s;
-                not_subnormal = s.mode != 2;
-                if (crank == 0) {
-                    if (nonfinite) raise_error(kErrNonfinite);
-                    if (A.scales) A.scales[static_cast<int64_t>(tid) * A.q.num_chunks + j] = s.s;
-                }
-            }
-            const bool fast = __syncthreads_and(not_subnormal) != 0;
-            if (tid < W) {
-                const ScaleQ s = sq[row_rank[tid]];
-                row_s[tid] = s.s;
-                row_c[tid] = s.mode == 1 ? (scaled ? __fmul_rn(inv, s.rcp) : s.rcp) : 0.0f;
-            }
-            __syncthreads();
-            const RowScales rs{row_s, row_c, row_rank, sq};
-
-            // ---- quantise, dequantise, sum, mean
-#pragma unroll
-            for (int q = 0; q < kPipeGroups; ++q) {
-                const int64_t gi = g.sl.g0 + tid + q * kPipeThreads;
-                if (gi < g.sl.g1) {
-                    const int64_t e0 = gi * VEC;
-                    const bool full = e0 >= g.sl.lo && e0 + VEC <= g.sl.hi;
-                    if (fast && g.uniform) {
-                        auto ld = [&](int k) { return v[q][k]; };
-                        if (tree)
-                            fast_group<DT, WC, CODES, true>(ld, W, rs, e0, full, g.sl.lo, g.sl.hi, A, pow2);
-                        else if (DT == 0)
-                            fast_group_f32x2<WC, CODES>(ld, W, rs, e0, full, g.sl.lo, g.sl.hi, A, pow2);
-                        else
-                            fast_group<DT, WC, CODES, false>(ld, W, rs, e0, full, g.sl.lo, g.sl.hi, A, pow2);
-                    } else {
-                        auto ldr = [&](int r) { return ld_global_nc_v16(grads + static_cast<int64_t>(r) * row_bytes + gi * 16); };
-                        general_group<DT, CODES>(ldr, W, sq, g.lo, g.seg, e0, full, g.sl.lo, g.sl.hi, A, pow2);
-                    }
-                }
-            }
-            for (int64_t gi = g.sl.g0 + tid + kPipeGroups * kPipeThreads; gi < g.sl.g1; gi += kPipeThreads) {
-                const int64_t e0 = gi * VEC;
-                const bool full = e0 >= g.sl.lo && e0 + VEC <= g.sl.hi;
-                auto ldr = [&](int r) { return ld_global_nc_v16(grads + static_cast<int64_t>(r) * row_bytes + gi * 16); };
-                general_group<DT, CODES>(ldr, W, sq, g.lo, g.seg, e0, full, g.sl.lo, g.sl.hi, A, pow2);
-            }
-        } else if (crank == 0 && tid == 0) {
-            raise_error(kErrBadTable);
-        }
-    }
-    // a copy still in flight (only after a wait ran out) lands before the CTA leaves
-    if (tid == 0 && pending) mbar_wait_bounded(&bar, phase & 1u, wait_limit);
 }
 
 // Per-rank staging capacity for a cluster of P: chunks up to 144 KiB per rank (dynamic_chunk
@@ -901,7 +595,7 @@ inline cudaError_t launch(DeviceInit* table, const QuantArgs& a, int order, floa
     const uint32_t P = cluster_size(a.W, di.cluster16);
     uint32_t row_cap = staging_row_cap(P);
     size_t smem = static_cast<size_t>(a.W) * row_cap;
-    if (smem > kMaxStagingBytes || kMaxStagingBytes == 0) {
+    if (smem > kMaxStagingBytes || kMaxStagingBytes == 0 || a.W == 8) {
         row_cap = 0;
         smem = 0;
     }
@@ -933,92 +627,6 @@ inline cudaError_t launch(DeviceInit* table, const QuantArgs& a, int order, floa
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return codes ? launch_codes<DT, true>(&cfg, A) : launch_codes<DT, false>(&cfg, A);
-}
-
-// ---------------------------------------------------------------- k_fused_pipe launcher (W = 8)
-
-struct RegInit {
-    std::once_flag once;
-    int clusters = 0;  // co-resident clusters of 16 (0: the kernel cannot run here)
-};
-
-template <int DT>
-inline void init_reg(RegInit* ri) {
-    const int smem = static_cast<int>(8 * staging_row_cap(16));
-    bool ok = true;
-    for (int c = 0; c < 2 && ok; ++c) {
-        auto fn = c ? k_fused_pipe<DT, 8, true> : k_fused_pipe<DT, 8, false>;
-        ok = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-             cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess;
-    }
-    if (!ok) cudaGetLastError();
-    int n = 0;
-    if (ok) {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 16;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(16);
-        cfg.blockDim = dim3(kPipeThreads);
-        cfg.dynamicSmemBytes = smem;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&n, k_fused_pipe<DT, 8, false>, &cfg) != cudaSuccess) {
-            cudaGetLastError();
-            n = 0;
-        }
-    }
-    ri->clusters = ok ? n : 0;
-}
-
-// Launches k_fused_pipe for W = 8 (clusters of 16 CTAs, two per ring segment, as many clusters as
-// are co-resident); otherwise sets *launched = false and the caller uses k_fused.
-template <int DT>
-inline cudaError_t launch_reg_dt(RegInit* table, const QuantArgs& a, int order, float* out, int8_t* codes,
-                                 float* scales, cudaStream_t stream, bool* launched) {
-    *launched = false;
-    if (a.W != 8) return cudaSuccess;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    RegInit& ri = table[dev];
-    std::call_once(ri.once, [&] { init_reg<DT>(&ri); });
-    if (ri.clusters <= 0) return cudaSuccess;
-    const uint32_t P = 16;
-#ifdef GQ_PIPE_ONE_CHUNK_PER_CLUSTER
-    const int64_t G = a.num_chunks;
-#else
-    const int64_t G = a.num_chunks < ri.clusters ? a.num_chunks : ri.clusters;
-#endif
-    Args A;
-    A.q = a;
-    A.order = order;
-    A.out = out;
-    A.codes = codes;
-    A.scales = scales;
-    A.row_cap = staging_row_cap(P);
-    A.P = P;
-    A.invW = 0.125f;
-    A.w_pow2 = 1;
-    A.ring_split = order == kOrderRing ? 1 : 0;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = P;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(G * P));
-    cfg.blockDim = dim3(kPipeThreads);
-    cfg.dynamicSmemBytes = 8 * A.row_cap;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    *launched = true;
-    return codes ? cudaLaunchKernelEx(&cfg, k_fused_pipe<DT, 8, true>, A)
-                 : cudaLaunchKernelEx(&cfg, k_fused_pipe<DT, 8, false>, A);
 }
 
 inline cudaError_t read_clear_error(unsigned* word) {

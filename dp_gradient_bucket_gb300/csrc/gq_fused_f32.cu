@@ -1,5 +1,4 @@
-// gq_fused_f32.cu -- the fused kernel for fp32 gradients: the persistent kernel for W = 8
-// (gq_reg_f32.cu) when it applies, else the staged / re-read cluster kernel k_fused (gq_fused.cuh).
+// gq_fused_f32.cu -- the cluster kernel k_fused (gq_fused.cuh) for fp32 gradients.
 #include "gq_fused.cuh"
 
 namespace gq {
@@ -8,11 +7,6 @@ static fused::DeviceInit g_init_f32[64];
 
 cudaError_t launch_fused_f32(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales,
                              cudaStream_t stream) {
-#ifndef GQ_NO_REG_KERNEL
-    bool launched = false;
-    const cudaError_t e = launch_reg_f32(a, order, out, codes, scales, stream, &launched);
-    if (launched || e != cudaSuccess) return e;
-#endif
     return fused::launch<0>(g_init_f32, a, order, out, codes, scales, stream);
 }
 

@@ -50,7 +50,7 @@ cudaError_t launch_fused(const QuantArgs& a, int order, float* out, int8_t* code
 
 // The same with a zero-filled workspace (gq_fused_allreduce_sim_ws): the work-queue kernel for W = 8.
 cudaError_t launch_fused_ws(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales,
-                            uint32_t* workspace, cudaStream_t stream);
+                            uint32_t* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 // Per-input-type halves of the fused kernel (gq_fused_f32.cu, gq_fused_f16.cu): launch, read
 // and clear their device error word (OR-ed into *word), set the fault-injection stall.
@@ -63,20 +63,12 @@ cudaError_t fused_f16_read_clear_error(unsigned* word);
 cudaError_t fused_f32_set_stall(uint32_t extra_bytes, uint64_t limit_ns);
 cudaError_t fused_f16_set_stall(uint32_t extra_bytes, uint64_t limit_ns);
 
-// The persistent kernel for W = 8 (gq_reg_f32.cu, gq_reg_f16.cu): *launched tells whether it
-// took the call.
-cudaError_t launch_reg_f32(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales,
-                           cudaStream_t stream, bool* launched);
-cudaError_t launch_reg_f16(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales,
-                           cudaStream_t stream, bool* launched);
-cudaError_t reg_f32_read_clear_error(unsigned* word);
-cudaError_t reg_f16_read_clear_error(unsigned* word);
 
 // The work-queue kernel for W = 8 (gq_queue_f32.cu, gq_queue_f16.cu) on a zero-filled workspace.
 cudaError_t launch_queue_f32(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales,
-                             uint32_t* workspace, cudaStream_t stream, bool* launched);
+                             uint32_t* workspace, size_t workspace_bytes, cudaStream_t stream, bool* launched);
 cudaError_t launch_queue_f16(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales,
-                             uint32_t* workspace, cudaStream_t stream, bool* launched);
+                             uint32_t* workspace, size_t workspace_bytes, cudaStream_t stream, bool* launched);
 cudaError_t queue_f32_read_clear_error(unsigned* word);
 cudaError_t queue_f16_read_clear_error(unsigned* word);
 cudaError_t queue_f32_set_stall(uint32_t extra_bytes, uint64_t limit_ns);

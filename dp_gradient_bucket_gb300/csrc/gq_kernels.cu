@@ -300,10 +300,11 @@ cudaError_t launch_fused(const QuantArgs& a, int order, float* out, int8_t* code
 }
 
 cudaError_t launch_fused_ws(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales,
-                            uint32_t* workspace, cudaStream_t stream) {
+                            uint32_t* workspace, size_t workspace_bytes, cudaStream_t stream) {
     bool launched = false;
-    const cudaError_t e = a.dt == 0 ? launch_queue_f32(a, order, out, codes, scales, workspace, stream, &launched)
-                                    : launch_queue_f16(a, order, out, codes, scales, workspace, stream, &launched);
+    const cudaError_t e =
+        a.dt == 0 ? launch_queue_f32(a, order, out, codes, scales, workspace, workspace_bytes, stream, &launched)
+                  : launch_queue_f16(a, order, out, codes, scales, workspace, workspace_bytes, stream, &launched);
     if (launched || e != cudaSuccess) return e;
     return launch_fused(a, order, out, codes, scales, stream);
 }
@@ -329,8 +330,6 @@ cudaError_t read_and_clear_error_word(unsigned* word, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if ((e = fused_f32_read_clear_error(&w)) != cudaSuccess) return e;
     if ((e = fused_f16_read_clear_error(&w)) != cudaSuccess) return e;
-    if ((e = reg_f32_read_clear_error(&w)) != cudaSuccess) return e;
-    if ((e = reg_f16_read_clear_error(&w)) != cudaSuccess) return e;
     if ((e = queue_f32_read_clear_error(&w)) != cudaSuccess) return e;
     if ((e = queue_f16_read_clear_error(&w)) != cudaSuccess) return e;
     *word = w;

@@ -3,23 +3,29 @@
 // Same arithmetic as gq_fused.cuh ("pipelined HCCL AllReduce" article, bjdmk.com.cn/news/6235379,
 // §2.1 chunks, §2.2.1 quantize_gradient + INT8_ALLREDUCE, §3.1 one SUM per chunk, §6.1 unscale;
 // mean as in the "torchtitan-npu 3D parallel" article, AMP + 3D section), scheduled so that HBM
-// streams without waiting for any chunk's absmax:
+// streams without any CTA waiting for a whole chunk's absmax:
 //
-//   - Each chunk is cut into S slices (S a multiple of W under the ring order, so a slice lies in
-//     one ring segment).  Work items are (pass, chunk, slice).
-//   - Pass 1 of a slice reads its W rank rows from HBM (L2 policy evict_last: the bytes are read
-//     again soon), reduces the per-rank absmax, folds it into a per-(chunk, rank) word with
-//     atomicMax, and counts the slice done for its chunk.
-//   - Pass 2 of a slice waits (bounded) until all S slices of its chunk finished pass 1, reads the W
-//     scales, reads the rows again (from L2, evict_first), quantises, dequantises, sums and stores.
-//   - Items are handed out in one global order by atomicAdd on a queue head: pass 1 of chunk k,
-//     then pass 2 of chunk k - L (L chunks of lag).  An item's dependencies are always handed out
-//     before it, to CTAs that are already running and wait on nothing, so the queue makes progress
-//     whatever the number of resident CTAs.  The lag keeps about L chunks of re-read data in L2 and
-//     hides the absmax hand-off.
-//   - The workspace (queue head, exit count, per-chunk counters, per-(chunk, rank) absmax words)
-//     must be zero when a launch starts; the last pass 2 of each chunk and the last CTA to leave
-//     zero it again, so consecutive launches need no clearing in between.
+//   - Each chunk is cut into S = 32 slices (under the ring order, S / W slices per ring segment, so a
+//     slice has one ring start).  Work items are (pass, chunk, slice).
+//   - Pass 1 of a slice reads its W rank rows (16-byte loads, L2 policy evict_last: they are read
+//     again soon), takes the per-rank absmax and publishes it: one 64-bit word per (chunk, slice,
+//     rank) holding the absmax bits and this launch's tag, written with a single store.
+//   - Pass 2 waits (bounded) until all S x W words of its chunk carry this launch's tag, takes the
+//     per-rank maximum, reads the rows again (from L2, evict_first), quantises, dequantises, sums
+//     and stores the mean.
+//   - Items are handed out in one global order by atomicAdd on a queue head, kQueueBatch at a time
+//     (the items of a claim share pass and chunk; the next claim is in flight while one is worked
+//     on): pass 1 of chunk k, then pass 2 of chunk k - L (L chunks of lag).  An item's dependencies
+//     are handed out before it and never wait on a later item, so the queue makes progress whatever
+//     the number of resident CTAs.  The lag keeps about L chunks of re-read data in L2 and hides
+//     the absmax hand-off.
+//   - No fence and no atomic read-modify-write sits on the data path: a published word carries
+//     its tag and value in one store, and a reader accepts only words with its launch's tag.
+//
+// Workspace: the queue head, an exit count, the launch epoch, then the (chunk, slice, rank) words.
+// It must be zero-filled before its first launch.  The last CTA to leave resets the head and the
+// count and advances the epoch, so a word published by an earlier launch never carries the tag of
+// a later one; consecutive launches need no clearing in between.
 #pragma once
 
 #include "gq_fused.cuh"
@@ -28,18 +34,35 @@ namespace gq {
 namespace fused {
 
 constexpr int kQueueThreads = 256;
-constexpr int kQueueSlices = 32;  // per chunk (a multiple of W = 8)
-constexpr int kQueueLag = 24;     // chunks between pass 1 and pass 2 of a chunk
+#ifndef GQ_QUEUE_MIN_CTAS
+#define GQ_QUEUE_MIN_CTAS 2
+#endif
+constexpr int kQueueSlices = 32;  // per chunk (a multiple of W = 8; one lane per slice when polling)
+#ifndef GQ_QUEUE_LAG
+#define GQ_QUEUE_LAG 64
+#endif
+constexpr int kQueueLag = GQ_QUEUE_LAG;  // chunks between pass 1 and pass 2 of a chunk
+#ifndef GQ_QUEUE_BATCH
+#define GQ_QUEUE_BATCH 4
+#endif
+constexpr int kQueueBatch = GQ_QUEUE_BATCH;  // items per claim; divides kQueueSlices
+constexpr int kQueueW = 8;
+static_assert(kQueueSlices == 32 && kQueueSlices % kQueueW == 0 && kQueueSlices % kQueueBatch == 0,
+              "slice geometry");
 
-// Workspace words: [0] queue head, [1] CTAs done, [2 + j] chunk j's counter (pass-1 slices done,
-// then pass-2 slices done on top), [2 + num_chunks + j * W + r] absmax bits of rank r in chunk j.
-inline size_t queue_workspace_words(int64_t num_chunks, int W) {
-    return 2 + static_cast<size_t>(num_chunks) + static_cast<size_t>(num_chunks) * W;
+// Workspace: 4 words of header ([0] queue head, [1] CTAs done, [2] epoch, [3] unused), then one
+// 64-bit word per (chunk j, slice t, rank r) at index (j * S + t) * W + r: (epoch + 1) << 32 | absmax
+// bits.  The tag epoch + 1 is never 0, so a zero-filled workspace holds no published word.
+constexpr size_t kQueueHeaderBytes = 16;
+inline size_t queue_workspace_bytes(int64_t num_chunks, int W) {
+    return kQueueHeaderBytes + static_cast<size_t>(num_chunks) * kQueueSlices * static_cast<size_t>(W) * 8;
 }
 
 struct QueueArgs {
     Args f;
-    uint32_t* ws;
+    uint32_t* ws;            // header words
+    uint64_t* slots;         // (chunk, slice, rank) words
+    size_t slot_words;       // words the workspace holds (all cleared when the epoch wraps)
     int64_t total_items;
     int lag;
 };
@@ -78,188 +101,263 @@ __device__ __forceinline__ V16 ld_global_hint_v16(const void* p, uint64_t policy
     return v;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
+__device__ __forceinline__ void ld_volatile_v2_u64(const uint64_t* p, uint64_t* a, uint64_t* b) {
+    asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(*a), "=l"(*b) : "l"(p) : "memory");
 }
 
-template <int DT, int WC, bool CODES>
-__global__ void __launch_bounds__(kQueueThreads, 3) k_queue(const QueueArgs Q) {
+__device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Slice `slice` of chunk [lo, hi) (length <= INT_MAX): its elements [slo, shi), its groups
+// [g0, g0 + ng) on the global 16-byte grid, and the ring start of its elements.  Under the ring
+// order the chunk's W segments (torch.chunk pieces of seg = ceil(len / W)) are cut into S / W
+// near-equal runs of groups each, so a slice lies in one segment; otherwise the chunk is cut into
+// S runs.  Every divisor is a compile-time constant.
+struct ItemGeom {
+    int64_t slo, shi, g0;
+    uint32_t ng;
+    int rot;
+};
+
+template <int VEC>
+__device__ __forceinline__ ItemGeom item_geom(bool ring_split, int64_t lo, int64_t hi, uint32_t seg, int slice) {
+    constexpr int W = kQueueW;
+    constexpr int S = kQueueSlices;
+    constexpr int SUB = S / W;
+    ItemGeom g;
+    int64_t a = lo, b = hi;
+    uint32_t c = static_cast<uint32_t>(slice);
+    g.rot = 0;
+    if (ring_split) {
+        const int t = slice / SUB;
+        a = min(hi, lo + static_cast<int64_t>(t) * seg);
+        b = min(hi, lo + static_cast<int64_t>(t + 1) * seg);
+        c = static_cast<uint32_t>(slice % SUB);
+        g.rot = (t + 1 == W) ? 0 : t + 1;
+    }
+    if (b <= a) {
+        g.slo = g.shi = a;
+        g.g0 = a / VEC;
+        g.ng = 0;
+        return g;
+    }
+    const int64_t G0 = a / VEC;
+    const uint32_t total = static_cast<uint32_t>((b + VEC - 1) / VEC - G0);
+    const uint32_t gs = ring_split ? (total + SUB - 1) / SUB : (total + S - 1) / S;
+    const uint32_t q0 = min(total, gs * c), q1 = min(total, gs * (c + 1));
+    g.g0 = G0 + q0;
+    g.ng = q1 - q0;
+    g.slo = max(a, g.g0 * VEC);
+    g.shi = min(b, (G0 + q1) * VEC);
+    if (g.shi <= g.slo) {
+        g.shi = g.slo;
+        g.ng = 0;
+    }
+    return g;
+}
+
+template <int DT, bool CODES>
+__global__ void __launch_bounds__(kQueueThreads, GQ_QUEUE_MIN_CTAS) k_queue(const QueueArgs Q) {
     constexpr int VEC = DT == 0 ? 4 : 8;
     constexpr int EB = DT == 0 ? 4 : 2;
-    constexpr int W = WC;
-    constexpr int NWARP = kQueueThreads / 32;
+    constexpr int W = kQueueW;
     constexpr int S = kQueueSlices;
+    constexpr int NWARP = kQueueThreads / 32;
     const Args& A = Q.f;
-    __shared__ int64_t s_item;
-    __shared__ uint32_t wmax[NWARP][W];
+    __shared__ uint32_t s_claim, s_tag;
+    __shared__ uint32_t wmax[2][NWARP][W];   // per-warp absmax partials, double-buffered by item
+    // the scales of the pass-2 chunk held: by rank (sq), and by row twice over, so that row k of a
+    // slice with ring start rot reads entry k + rot
     __shared__ ScaleQ sq[W];
-    __shared__ float row_s[W], row_c[W];
-    __shared__ int row_rank[W];
-    __shared__ int s_ok;
+    __shared__ float dup_s[2 * W], dup_c[2 * W];
+    __shared__ int dup_rank[2 * W];
+    __shared__ int s_fast, s_ok, s_nonfinite[W];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t n = A.q.num_chunks;
     uint32_t* head = Q.ws;
-    uint32_t* done = Q.ws + 1;
-    uint32_t* counter = Q.ws + 2;
-    uint32_t* amax = Q.ws + 2 + n;
     const char* grads = static_cast<const char*>(A.q.grads);
     const int64_t row_bytes = A.q.rank_stride * EB;
     const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
-    const uint64_t wait_limit = g_wait_limit_ns;
-    const bool pow2 = (W & (W - 1)) == 0;
     const float inv = A.q.inv;
     const bool scaled = A.q.scaled != 0;
+    const bool ring_split = A.ring_split != 0;
+    const bool tree = A.order == kOrderTree;
+    const bool pow2 = true;  // W = 8
+
+    if (tid == 0) {
+        // the epoch moves only after every CTA of this launch has left, so all CTAs read one value
+        s_tag = *reinterpret_cast<volatile uint32_t*>(Q.ws + 2) + 1u;
+        s_claim = atomicAdd(head, static_cast<uint32_t>(kQueueBatch));
+    }
+    __syncthreads();
+    const uint32_t tag = s_tag;
+    const uint64_t wait_limit = g_wait_limit_ns;
+    int64_t cached = -1;  // chunk whose scales the shared tables hold
+    bool failed = false;
+    int parity = 0;
 
     for (;;) {
-        if (tid == 0) s_item = static_cast<int64_t>(atomicAdd(head, 1u));
-        __syncthreads();
-        const int64_t item = s_item;
-        __syncthreads();  // s_item is read by everyone before thread 0 may overwrite it
-        if (item >= Q.total_items) break;
-        int pass, slice;
+        const int64_t base = s_claim;
+        if (base >= Q.total_items || failed) break;
+        uint32_t next = 0;
+        if (tid == 0) next = atomicAdd(head, static_cast<uint32_t>(kQueueBatch));  // used after this batch
+        int pass, slice0;
         int64_t j;
-        queue_item(item, n, Q.lag, &pass, &j, &slice);
+        queue_item(base, n, Q.lag, &pass, &j, &slice0);
         int64_t lo, hi;
-        if (!chunk_bounds(A.q.offsets, j, n, A.q.rank_stride, &lo, &hi)) {
-            if (tid == 0 && pass == 0 && slice == 0) raise_error(kErrBadTable);
-            continue;
-        }
+        const bool good = chunk_bounds(A.q.offsets, j, n, A.q.rank_stride, &lo, &hi);
+        if (!good && tid == 0 && pass == 0 && slice0 == 0) raise_error(kErrBadTable);
         const uint32_t seg = hi > lo ? static_cast<uint32_t>((hi - lo + W - 1) / W) : 1u;
-        // slice `slice` of S: S / W slices per ring segment under the ring order, else S equal runs
-        Slice sl;
-        if (A.ring_split) {
-            const int sub = S / W;
-            const int64_t t = slice / sub;
-            const int64_t a = min(hi, lo + t * seg), b = min(hi, lo + (t + 1) * seg);
-            sl = split_range<VEC>(a, b, static_cast<uint32_t>(slice % sub), static_cast<uint32_t>(sub));
-        } else {
-            sl = split_range<VEC>(lo, hi, static_cast<uint32_t>(slice), static_cast<uint32_t>(S));
-        }
-        int rot = 0;
-        bool uniform = true;
-        if (A.order == kOrderRing && sl.hi > sl.lo) {
-            const int t0 = segment_of(sl.lo, lo, seg), t1 = segment_of(sl.hi - 1, lo, seg);
-            uniform = t0 == t1;
-            if (uniform) rot = (t0 + 1 == W) ? 0 : t0 + 1;
+        const int nb = static_cast<int>(min(static_cast<int64_t>(kQueueBatch), Q.total_items - base));
+
+        if (good && pass == 1 && j != cached) {
+            // warp 0: wait until all S x W words of chunk j carry this launch's tag; lane t reads slice t.
+            // A CTA waits here only between claims, holding no unpublished absmax, so the CTA that
+            // holds the oldest waiting claim always finds its words published in the end.
+            if (warp == 0) {
+                const uint64_t* words = Q.slots + (static_cast<size_t>(j) * S + lane) * W;
+                uint32_t mx[W];
+                uint64_t t0 = 0;
+                int ok = 1;
+                for (int tries = 0;; ++tries) {
+                    uint64_t w[W];
+#pragma unroll
+                    for (int k = 0; k < W; k += 2) ld_volatile_v2_u64(words + k, &w[k], &w[k + 1]);
+                    bool mine = true;
+#pragma unroll
+                    for (int k = 0; k < W; ++k) {
+                        mine &= static_cast<uint32_t>(w[k] >> 32) == tag;
+                        mx[k] = static_cast<uint32_t>(w[k]);
+                    }
+                    if (__all_sync(0xffffffffu, mine)) break;
+                    if (tries == 0) t0 = global_timer_ns();
+                    const int late = global_timer_ns() - t0 > wait_limit;
+                    if (__shfl_sync(0xffffffffu, late, 0)) {
+                        ok = 0;
+                        break;
+                    }
+                    __nanosleep(100);
+                }
+                uint32_t mraw = 0;
+#pragma unroll
+                for (int k = 0; k < W; ++k) {
+                    const uint32_t m = __reduce_max_sync(0xffffffffu, mx[k]);
+                    if (lane == k) mraw = m;
+                }
+                bool not_subnormal = true;
+                if (lane < W) {
+                    float m = DT == 0 ? __uint_as_float(mraw)
+                                      : __half2float(__ushort_as_half(static_cast<unsigned short>(mraw)));
+                    if (scaled) m = __fmul_rn(m, inv);  // max|fl(x*inv)| = fl(max|x| * inv)
+                    const ScaleQ q = make_scale(m);
+                    sq[lane] = q;
+                    not_subnormal = q.mode != 2;
+                    s_nonfinite[lane] =
+                        (DT == 0 ? mraw >= 0x7f800000u : mraw >= 0x7c00u) || !(fabsf(m) <= 3.40282347e38f);
+                    const float c = q.mode == 1 ? (scaled ? __fmul_rn(inv, q.rcp) : q.rcp) : 0.0f;
+                    dup_s[lane] = dup_s[lane + W] = q.s;
+                    dup_c[lane] = dup_c[lane + W] = c;
+                    dup_rank[lane] = dup_rank[lane + W] = lane;
+                }
+                const bool fast = __all_sync(0xffffffffu, not_subnormal);
+                if (lane == 0) {
+                    s_fast = fast;
+                    s_ok = ok;
+                    if (!ok) raise_error(kErrTimeout);
+                }
+            }
+            __syncthreads();
+            cached = j;
+            if (!s_ok) failed = true;  // the chunk's scales are unknown: this CTA stops
         }
 
-        if (pass == 0) {
-            // ---------------------------------------------------------------- pass 1: absmax
-            uint32_t mx[W];
+        for (int b = 0; good && !failed && b < nb; ++b) {
+            const int slice = slice0 + b;
+            const ItemGeom g = item_geom<VEC>(ring_split, lo, hi, seg, slice);
+            if (pass == 0) {
+                uint32_t mx[W];
 #pragma unroll
-            for (int k = 0; k < W; ++k) mx[k] = 0;
-            for (int64_t g = sl.g0 + tid; g < sl.g1; g += kQueueThreads) {
-                const int64_t e0 = g * VEC;
-                const bool full = e0 >= sl.lo && e0 + VEC <= sl.hi;
-                V16 v[W];
-#pragma unroll
-                for (int k = 0; k < W; ++k) v[k] = ld_global_hint_v16(grads + k * row_bytes + g * 16, keep);
-#pragma unroll
-                for (int k = 0; k < W; ++k) mx[k] = group_absmax<DT>(v[k], e0, full, sl.lo, sl.hi, mx[k]);
-            }
-#pragma unroll
-            for (int k = 0; k < W; ++k) {
-                const uint32_t m = __reduce_max_sync(0xffffffffu, mx[k]);
-                if (lane == 0) wmax[warp][k] = m;
-            }
-            __syncthreads();
-            if (tid < W) {
-                uint32_t m = 0;
-#pragma unroll
-                for (int w = 0; w < NWARP; ++w) m = max(m, wmax[w][tid]);
-                if (m != 0) atomicMax(amax + j * W + tid, m);
-                __threadfence();  // this thread's absmax update before the count below
-            }
-            __syncthreads();
-            if (tid == 0) {
-                __threadfence();  // the absmax words before the count that publishes them
-                atomicAdd(counter + j, 1u);
-            }
-        } else {
-            // ---------------------------------------------------------------- pass 2: reduce
-            if (tid == 0) {
-                int ok = 1;
-                if (ld_acquire_gpu_u32(counter + j) < static_cast<uint32_t>(S)) {
-                    const uint64_t t0 = global_timer_ns();
-                    while (ld_acquire_gpu_u32(counter + j) < static_cast<uint32_t>(S)) {
-                        if (global_timer_ns() - t0 > wait_limit) {
-                            raise_error(kErrTimeout);
-                            ok = 0;
-                            break;
-                        }
-                        __nanosleep(200);
-                    }
-                }
-                s_ok = ok;
-                // the thread that acquired the count reads the chunk's absmax words for everyone
-#pragma unroll
-                for (int r = 0; r < W; ++r) wmax[0][r] = ld_acquire_gpu_u32(amax + j * W + r);
-            }
-            __syncthreads();
-            bool not_subnormal = true;
-            if (tid < W) {
-                const uint32_t mraw = wmax[0][tid];
-                float m = DT == 0 ? __uint_as_float(mraw)
-                                  : __half2float(__ushort_as_half(static_cast<unsigned short>(mraw)));
-                if (scaled) m = __fmul_rn(m, inv);  // max|fl(x*inv)| = fl(max|x| * inv)
-                const bool nonfinite = (DT == 0 ? mraw >= 0x7f800000u : mraw >= 0x7c00u) || !(fabsf(m) <= 3.40282347e38f);
-                const ScaleQ s = make_scale(m);
-                sq[tid] = s;
-                not_subnormal = s.mode != 2;
-                if (slice == 0) {
-                    if (nonfinite) raise_error(kErrNonfinite);
-                    if (A.scales) A.scales[static_cast<int64_t>(tid) * n + j] = s.s;
-                }
-            }
-            const bool fast = __syncthreads_and(not_subnormal) != 0;
-            if (tid < W) {
-                const int r = (tid + rot) % W;
-                row_rank[tid] = r;
-                const ScaleQ s = sq[r];
-                row_s[tid] = s.s;
-                row_c[tid] = s.mode == 1 ? (scaled ? __fmul_rn(inv, s.rcp) : s.rcp) : 0.0f;
-            }
-            __syncthreads();
-            const RowScales rs{row_s, row_c, row_rank, sq};
-            for (int64_t g = sl.g0 + tid; g < sl.g1; g += kQueueThreads) {
-                const int64_t e0 = g * VEC;
-                const bool full = e0 >= sl.lo && e0 + VEC <= sl.hi;
-                if (fast && uniform) {
+                for (int k = 0; k < W; ++k) mx[k] = 0;
+                for (uint32_t gi = tid; gi < g.ng; gi += kQueueThreads) {
+                    const int64_t grp = g.g0 + gi;
+                    const int64_t e0 = grp * VEC;
+                    const bool full = e0 >= g.slo && e0 + VEC <= g.shi;
                     V16 v[W];
 #pragma unroll
-                    for (int k = 0; k < W; ++k)
-                        v[k] = ld_global_hint_v16(grads + static_cast<int64_t>((k + rot) % W) * row_bytes + g * 16, drop);
-                    auto ld = [&](int k) { return v[k]; };
-                    if (A.order == kOrderTree)
-                        fast_group<DT, WC, CODES, true>(ld, W, rs, e0, full, sl.lo, sl.hi, A, pow2);
-                    else if (DT == 0)
-                        fast_group_f32x2<WC, CODES>(ld, W, rs, e0, full, sl.lo, sl.hi, A, pow2);
-                    else
-                        fast_group<DT, WC, CODES, false>(ld, W, rs, e0, full, sl.lo, sl.hi, A, pow2);
-                } else {
-                    auto ldr = [&](int r) { return ld_global_nc_v16(grads + static_cast<int64_t>(r) * row_bytes + g * 16); };
-                    general_group<DT, CODES>(ldr, W, sq, lo, seg, e0, full, sl.lo, sl.hi, A, pow2);
+                    for (int k = 0; k < W; ++k) v[k] = ld_global_hint_v16(grads + k * row_bytes + grp * 16, keep);
+#pragma unroll
+                    for (int k = 0; k < W; ++k) mx[k] = group_absmax<DT>(v[k], e0, full, g.slo, g.shi, mx[k]);
                 }
-            }
-            __syncthreads();
-            if (tid == 0) {
-                // the last pass-2 slice of the chunk clears its counter and absmax words for the next launch
-                if (atomicAdd(counter + j, 1u) == static_cast<uint32_t>(2 * S - 1)) {
-                    for (int r = 0; r < W; ++r) amax[j * W + r] = 0;
-                    counter[j] = 0;
+#pragma unroll
+                for (int k = 0; k < W; ++k) {
+                    const uint32_t m = __reduce_max_sync(0xffffffffu, mx[k]);
+                    if (lane == k) wmax[parity][warp][k] = m;
+                }
+                __syncthreads();
+                if (tid < W) {
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int w2 = 0; w2 < NWARP; ++w2) m = max(m, wmax[parity][w2][tid]);
+                    // tag and value in one store: a reader never sees one without the other
+                    st_relaxed_gpu_u64(Q.slots + (static_cast<size_t>(j) * S + slice) * W + tid,
+                                       (static_cast<uint64_t>(tag) << 32) | m);
+                }
+                parity ^= 1;
+            } else {
+                if (slice == 0 && tid < W) {
+                    if (s_nonfinite[tid]) raise_error(kErrNonfinite);
+                    if (A.scales) A.scales[static_cast<int64_t>(tid) * n + j] = sq[tid].s;
+                }
+                const int rot = g.rot;
+                const RowScales rs{dup_s + rot, dup_c + rot, dup_rank + rot, sq};
+                const bool fast = s_fast != 0;
+                for (uint32_t gi = tid; gi < g.ng; gi += kQueueThreads) {
+                    const int64_t grp = g.g0 + gi;
+                    const int64_t e0 = grp * VEC;
+                    const bool full = e0 >= g.slo && e0 + VEC <= g.shi;
+                    if (fast) {
+                        V16 v[W];
+#pragma unroll
+                        for (int k = 0; k < W; ++k) {
+                            const int r = k + rot < W ? k + rot : k + rot - W;
+                            v[k] = ld_global_hint_v16(grads + r * row_bytes + grp * 16, drop);
+                        }
+                        auto ld = [&](int k) { return v[k]; };
+                        if (tree)
+                            fast_group<DT, W, CODES, true>(ld, W, rs, e0, full, g.slo, g.shi, A, pow2);
+                        else
+                            fast_group<DT, W, CODES, false>(ld, W, rs, e0, full, g.slo, g.shi, A, pow2);
+                    } else {
+                        auto ldr = [&](int r) { return ld_global_nc_v16(grads + r * row_bytes + grp * 16); };
+                        general_group<DT, CODES>(ldr, W, sq, lo, seg, e0, full, g.slo, g.shi, A, pow2);
+                    }
                 }
             }
         }
+        // the next claim; the barrier also keeps the shared scale tables until every thread is done
+        if (tid == 0) s_claim = next;
+        __syncthreads();
     }
-    // the last CTA out resets the queue for the next launch: nobody takes items any more
+
+    // the last CTA out resets the queue and advances the epoch for the next launch
+    __shared__ int s_last;
     if (tid == 0) {
         __threadfence();
-        if (atomicAdd(done, 1u) == gridDim.x - 1) {
-            *head = 0;
-            *done = 0;
+        s_last = atomicAdd(Q.ws + 1, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+        if (tag == 0xffffffffu) {
+            // the tag space wrapped: clear every word so no old tag can match a later launch
+            for (size_t i = tid; i < Q.slot_words; i += blockDim.x) Q.slots[i] = 0;
+            __syncthreads();
+        }
+        if (tid == 0) {
+            Q.ws[0] = 0;
+            Q.ws[1] = 0;
+            Q.ws[2] = tag == 0xffffffffu ? 0u : tag;  // the next launch tags with tag + 1
             __threadfence();
         }
     }
@@ -267,7 +365,7 @@ __global__ void __launch_bounds__(kQueueThreads, 3) k_queue(const QueueArgs Q) {
 
 struct QueueInit {
     std::once_flag once;
-    int ctas = 0;  // resident CTAs of k_queue<DT, 8, false> on this device
+    int ctas = 0;  // resident CTAs of k_queue on this device (0: not usable)
 };
 
 template <int DT>
@@ -275,8 +373,7 @@ inline void init_queue(QueueInit* qi) {
     int per_sm = 0, sms = 0, dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_queue<DT, 8, false>, kQueueThreads, 0) !=
-            cudaSuccess) {
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_queue<DT, false>, kQueueThreads, 0) != cudaSuccess) {
         cudaGetLastError();
         qi->ctas = 0;
         return;
@@ -284,20 +381,27 @@ inline void init_queue(QueueInit* qi) {
     qi->ctas = per_sm * sms;
 }
 
-// Launches k_queue for W = 8 on a zero-filled workspace of queue_workspace_words(num_chunks, 8)
-// words; *launched = false when W != 8.
+// Launches k_queue for W = 8 on a workspace of ws_bytes >= queue_workspace_bytes(num_chunks, 8)
+// (zero-filled before its first launch); *launched = false when W != 8 or the kernel cannot run
+// on this device.
 template <int DT>
 inline cudaError_t launch_queue_dt(QueueInit* table, const QuantArgs& a, int order, float* out, int8_t* codes,
-                                   float* scales, uint32_t* ws, cudaStream_t stream, bool* launched) {
+                                   float* scales, uint32_t* ws, size_t ws_bytes, cudaStream_t stream,
+                                   bool* launched) {
     *launched = false;
-    if (a.W != 8) return cudaSuccess;
+    if (a.W != kQueueW) return cudaSuccess;
+    const int64_t total = 2 * static_cast<int64_t>(kQueueSlices) * a.num_chunks;
+    // the 32-bit queue head overshoots the item count by at most two claims per CTA
+    if (total + static_cast<int64_t>(kQueueBatch) * 2 * 65536 > static_cast<int64_t>(UINT_MAX)) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     QueueInit& qi = table[dev];
     std::call_once(qi.once, [&] { init_queue<DT>(&qi); });
-    if (qi.ctas <= 0) return cudaSuccess;
+    if (qi.ctas <= 0 || qi.ctas > 65536) return cudaSuccess;
+    *launched = true;
+    if (total == 0) return cudaSuccess;
     QueueArgs Q;
     Q.f.q = a;
     Q.f.order = order;
@@ -310,16 +414,14 @@ inline cudaError_t launch_queue_dt(QueueInit* table, const QuantArgs& a, int ord
     Q.f.w_pow2 = 1;
     Q.f.ring_split = order == kOrderRing ? 1 : 0;
     Q.ws = ws;
-    Q.total_items = 2 * static_cast<int64_t>(kQueueSlices) * a.num_chunks;
-#ifdef GQ_QUEUE_LAG
-    Q.lag = GQ_QUEUE_LAG;
-#else
+    Q.slots = reinterpret_cast<uint64_t*>(reinterpret_cast<char*>(ws) + kQueueHeaderBytes);
+    Q.slot_words = (ws_bytes - kQueueHeaderBytes) / 8;
+    Q.total_items = total;
     Q.lag = kQueueLag;
-#endif
-    const int64_t want = Q.total_items < qi.ctas ? Q.total_items : qi.ctas;
-    *launched = true;
-    if (codes) k_queue<DT, 8, true><<<static_cast<unsigned>(want), kQueueThreads, 0, stream>>>(Q);
-    else k_queue<DT, 8, false><<<static_cast<unsigned>(want), kQueueThreads, 0, stream>>>(Q);
+    const int64_t claims = (total + kQueueBatch - 1) / kQueueBatch;
+    const unsigned grid = static_cast<unsigned>(claims < qi.ctas ? claims : qi.ctas);
+    if (codes) k_queue<DT, true><<<grid, kQueueThreads, 0, stream>>>(Q);
+    else k_queue<DT, false><<<grid, kQueueThreads, 0, stream>>>(Q);
     return cudaGetLastError();
 }
 

@@ -6,8 +6,10 @@ namespace gq {
 static fused::QueueInit g_queue_init_f16[64];
 
 cudaError_t launch_queue_f16(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales,
-                            uint32_t* workspace, cudaStream_t stream, bool* launched) {
-    return fused::launch_queue_dt<1>(g_queue_init_f16, a, order, out, codes, scales, workspace, stream, launched);
+                             uint32_t* workspace, size_t workspace_bytes, cudaStream_t stream,
+                             bool* launched) {
+    return fused::launch_queue_dt<1>(g_queue_init_f16, a, order, out, codes, scales, workspace, workspace_bytes,
+                                     stream, launched);
 }
 
 cudaError_t queue_f16_read_clear_error(unsigned* word) { return fused::read_clear_error(word); }

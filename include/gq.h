@@ -135,32 +135,35 @@ gq_status gq_reduce_dequant(const int8_t* d_codes, const float* d_scales, int W,
                             size_t rank_stride, const int64_t* d_offsets, size_t num_chunks,
                             gq_order order, float* d_out, gq_stream_t stream);
 
-/* gq_quantize then gq_reduce_dequant in one pass over the gradients: every chunk's W rows
- * are staged on chip once (TMA bulk copies into shared memory of a thread-block cluster
- * that splits the chunk; the clusters exchange per-rank absmax through distributed shared
- * memory), so the gradients are read from HBM once and the codes never leave the chip.
- * Output bits equal those of the two calls above.  d_codes_opt / d_scales_opt, when not
- * NULL, also receive the codes and scales. */
+/* gq_quantize then gq_reduce_dequant in one kernel: a thread-block cluster splits each chunk,
+ * its CTAs exchange per-rank absmax through distributed shared memory, and the codes never
+ * leave the chip.  A CTA's share of the W rows is read from HBM once; the second read, after
+ * the exchange, comes from shared memory (bulk copies, W != 8) or from L2 (W = 8, where three
+ * small CTAs per SM ran faster than staging).  Output bits equal those of the two calls
+ * above.  d_codes_opt / d_scales_opt, when not NULL, also receive the codes and scales. */
 gq_status gq_fused_allreduce_sim(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
                                  const int64_t* d_offsets, size_t num_chunks, float loss_scale,
                                  gq_order order, float* d_out, int8_t* d_codes_opt,
                                  float* d_scales_opt, gq_stream_t stream);
 
 /* Bytes of device workspace gq_fused_allreduce_sim_ws needs for a chunk table of num_chunks chunks
- * and W ranks (4 * (2 + num_chunks * (W + 1))). */
+ * and W ranks: 16 + num_chunks * 32 * W * 8 (a 16-byte header and one 8-byte word per chunk,
+ * slice and rank; 2 KiB per chunk at W = 8, 0.2% of the 1 MiB of fp32 gradients it covers). */
 size_t gq_fused_workspace_bytes(size_t num_chunks, int W);
 
 /* gq_fused_allreduce_sim with a caller-owned device workspace: same arguments, same results bit for
  * bit.  For W = 8 it runs the pass over HBM as a work queue that needs no thread-block clusters:
  * per-slice absmax items stream the gradients from HBM, and per-slice reduce items read them back
- * from L2 once their chunk's absmax is settled (a small wait on a per-chunk count, bounded in time).
+ * from L2 once their chunk's absmax words are all published (a wait bounded in time).
  * For other W it runs the kernel of gq_fused_allreduce_sim and leaves the workspace alone.
  *   d_workspace      device memory of at least gq_fused_workspace_bytes(num_chunks, W) bytes,
  *                    16-byte aligned, ZERO-FILLED before its first use (one cudaMemset after
- *                    allocation).  A call that completes normally leaves it zero-filled again, so it
- *                    can be reused call after call; after a call that reported GQ_ERR_TIMEOUT or
- *                    GQ_ERR_BAD_TABLE it must be zero-filled again.  Calls that share a workspace
- *                    must not overlap on the device (use one stream, or one workspace per stream).
+ *                    allocation).  It carries state from call to call (a launch counter that tags
+ *                    the published words): pass it unchanged to the next call; a call that
+ *                    completes, even one that reports GQ_ERR_BAD_TABLE or GQ_WARN_NONFINITE,
+ *                    leaves it ready for the next.  After GQ_ERR_TIMEOUT zero-fill it again.
+ *                    Calls that share a workspace must not overlap on the device (use one
+ *                    stream, or one workspace per stream).
  *   workspace_bytes  its size; GQ_ERR_INVALID_ARG if it is short. */
 gq_status gq_fused_allreduce_sim_ws(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
                                     const int64_t* d_offsets, size_t num_chunks, float loss_scale,

@@ -346,3 +346,121 @@ def test_non_default_stream_and_fp32_loss_scale():
         assert gq.gq_get_error(s) == gq.GQ_OK
     want = oracle.fused(host, W, stride, oracle.plan_chunks([n], 4), oracle.RING, 1024.0)[0]
     H.assert_bits_equal(out.cpu().numpy(), want, "output")
+
+
+# ------------------------------------------------------------------ the workspace entry point (W = 8)
+
+@pytest.mark.parametrize("order,oorder", ORDERS)
+def test_ws_large_unaligned_chunks(order, oorder):
+    """A hand-made table with chunks far longer than dynamic_chunk makes them (a slice then spans
+    several shared-memory stages), chunk starts off the 16-byte grid, a 3-element chunk and an
+    empty one; both entry points against the oracle, bit for bit."""
+    W, n = 8, 460000
+    stride = gq.row_stride(n, 4)
+    host = np.zeros(W * stride, dtype=np.float32)
+    for r in range(W):
+        wl.fill(2, r, 0, n, host[r * stride:r * stride + n])
+    table = np.array([0, 3, 200003, 200010, 450001, 450001, 460000], dtype=np.int64)
+    for mode in ("fused_ws", "fused"):
+        out, codes, scales, _, st = H.run(host, W, stride, None, order, mode=mode, offsets=table)
+        assert st == gq.GQ_OK
+        H.compare_full(host, W, stride, table, oorder, 1.0, out[:n], codes, scales)
+
+
+def test_ws_fp16_unscale():
+    """fp16 gradients at W = 8 with loss scales 65536 and 3, every order."""
+    W, n = 8, 300007
+    stride = gq.row_stride(n, 2)
+    host = np.zeros(W * stride, dtype=np.float16)
+    for r in range(W):
+        wl.fill(4, r, 0, n, host[r * stride:r * stride + n])
+    for ls in (65536.0, 3.0):
+        for order, oorder in ORDERS:
+            out, codes, scales, off, st = H.run(host, W, stride, [n], order, loss_scale=ls, mode="fused_ws")
+            assert st == gq.GQ_OK
+            H.compare_full(host, W, stride, off, oorder, ls, out, codes, scales)
+
+
+def test_ws_nonfinite_input_is_reported():
+    W, n = 8, 300000
+    stride = gq.row_stride(n, 4)
+    host = np.zeros(W * stride, dtype=np.float32)
+    for r in range(W):
+        wl.fill(1, r, 0, n, host[r * stride:r * stride + n])
+    host[1 * stride + 5] = np.inf
+    host[6 * stride + 200000] = np.nan
+    off = oracle.plan_chunks([n], 4)
+    out, codes, scales, _, st = H.run(host, W, stride, [n], "ring", mode="fused_ws")
+    assert st == gq.GQ_WARN_NONFINITE
+    want = oracle.fused(host, W, stride, off, oracle.RING)[0]
+    bad = {0, int(np.searchsorted(off, 200000, side="right") - 1)}
+    for j in range(len(off) - 1):
+        if j not in bad:
+            H.assert_bits_equal(out[off[j]:off[j + 1]], want[off[j]:off[j + 1]], "finite chunk %d" % j)
+
+
+def test_ws_many_calls_and_workspace_after_bad_table():
+    """Ten calls in a row on one workspace give the same bits (the words of one call are never
+    taken for the next one's); after a call that reports a bad table the workspace still serves
+    the next call; a different table on the same workspace works too."""
+    W, n = 8, 1 << 20
+    host, stride = wl.rows(5, W, n)
+    dev = torch.device("cuda:0")
+    grads = torch.from_numpy(host).to(dev)
+    nc, d_off = H.plan_device([n], 4, dev)
+    want = oracle.fused(host, W, stride, d_off.cpu().numpy(), oracle.RING)[0]
+    ws = torch.zeros(gq.gq_fused_workspace_bytes(nc, W) // 4, dtype=torch.int32, device=dev)
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+
+    def check():
+        out.fill_(0)
+        gq.gq_fused_allreduce_sim_ws(grads, W, stride, d_off, nc, 1.0, "ring", out, ws)
+        assert gq.gq_get_error() == gq.GQ_OK
+        H.assert_bits_equal(out.cpu().numpy(), want, "output")
+        assert int(ws[0].item()) == 0 and int(ws[1].item()) == 0
+
+    for k in range(10):
+        check()
+        assert int(ws[2].item()) == k + 1  # one launch counted per call
+    bad = torch.tensor([0, 1000, 5000, 2000, 3000], dtype=torch.int64, device=dev)
+    gq.gq_fused_allreduce_sim_ws(grads, W, stride, bad, 4, 1.0, "ring", out, ws)
+    assert gq.gq_get_error() == gq.GQ_ERR_BAD_TABLE
+    check()
+    # a smaller table on the same workspace, then the original again
+    small = np.array([0, 40000, 70001, 70001, 100003], dtype=np.int64)
+    d_small = torch.from_numpy(small).to(dev)
+    gq.gq_fused_allreduce_sim_ws(grads, W, stride, d_small, 4, 1.0, "seq", out, ws)
+    assert gq.gq_get_error() == gq.GQ_OK
+    sub = host.reshape(W, stride)[:, :100003]
+    s2 = gq.row_stride(100003, 4)
+    rows = np.zeros((W, s2), dtype=np.float32)
+    rows[:, :100003] = sub
+    H.assert_bits_equal(out.cpu().numpy()[:100003], oracle.fused(rows.reshape(-1), W, s2, small, oracle.SEQ)[0],
+                        "small table")
+    check()
+
+
+def test_ws_epoch_wrap_clears_words():
+    """A workspace whose launch counter is one short of wrapping: that call clears every word and
+    restarts the counter, and the calls on either side of the wrap give the same bits."""
+    W, n = 8, 300001
+    host, stride = wl.rows(1, W, n)
+    dev = torch.device("cuda:0")
+    grads = torch.from_numpy(host).to(dev)
+    nc, d_off = H.plan_device([n], 4, dev)
+    want = oracle.fused(host, W, stride, d_off.cpu().numpy(), oracle.SEQ)[0]
+    ws = torch.zeros(gq.gq_fused_workspace_bytes(nc, W) // 4, dtype=torch.int32, device=dev)
+    out = torch.empty(n, dtype=torch.float32, device=dev)
+    gq.gq_fused_allreduce_sim_ws(grads, W, stride, d_off, nc, 1.0, "seq", out, ws)
+    assert gq.gq_get_error() == gq.GQ_OK
+    ws[2] = -2  # launch counter 0xfffffffe: the next call tags its words 0xffffffff
+    for k in range(3):
+        out.fill_(0)
+        gq.gq_fused_allreduce_sim_ws(grads, W, stride, d_off, nc, 1.0, "seq", out, ws)
+        assert gq.gq_get_error() == gq.GQ_OK
+        H.assert_bits_equal(out.cpu().numpy(), want, "output %d" % k)
+        if k == 0:
+            assert int(ws[2].item()) == 0
+            assert int(ws[4:].abs().sum().item()) == 0  # every word cleared
+        else:
+            assert int(ws[2].item()) == k
