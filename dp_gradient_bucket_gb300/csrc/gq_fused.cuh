@@ -12,8 +12,9 @@
 // k_fused: one chunk per thread-block cluster, CTA p of the cluster owning slice p.  For W other
 // than 8 the slice is bulk-copied into shared memory (TMA) when it fits; for W = 8 (compiled for
 // that W), and for slices that do not fit, it is read twice from global memory, the second time
-// from L2: on GB300 the re-read form ran the 25 MiB W = 8 bucket in 92 us against 164 us staged,
-// its CTAs being small enough for three to share an SM.
+// from L2, with one CTA per ring segment: on GB300 that form ran the 25 MiB W = 8 bucket in
+// 92 us, against 164 us staged (clusters of 16), its CTAs being small enough for three to share
+// an SM.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -592,12 +593,15 @@ inline cudaError_t launch(DeviceInit* table, const QuantArgs& a, int order, floa
     std::call_once(di.once, [&] { di.err = init_device<DT>(&di.cluster16); });
     if (di.err != cudaSuccess) return di.err;
 
-    const uint32_t P = cluster_size(a.W, di.cluster16);
+    uint32_t P = cluster_size(a.W, di.cluster16);
     uint32_t row_cap = staging_row_cap(P);
     size_t smem = static_cast<size_t>(a.W) * row_cap;
     if (smem > kMaxStagingBytes || kMaxStagingBytes == 0 || a.W == 8) {
         row_cap = 0;
         smem = 0;
+        // Re-read form: one CTA per ring segment (its clusters are half the size, and on GB300 the
+        // W = 8 bucket ran in 92 us with clusters of 8 against 131 us with clusters of 16).
+        if (static_cast<uint32_t>(a.W) <= (di.cluster16 ? 16u : 8u)) P = static_cast<uint32_t>(a.W);
     }
     const int64_t grid = a.num_chunks * P;
     if (grid > INT_MAX) return cudaErrorInvalidValue;

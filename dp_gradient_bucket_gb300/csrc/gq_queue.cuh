@@ -163,10 +163,13 @@ __global__ void __launch_bounds__(kQueueThreads, GQ_QUEUE_MIN_CTAS) k_queue(cons
     constexpr int EB = DT == 0 ? 4 : 2;
     constexpr int W = kQueueW;
     constexpr int S = kQueueSlices;
-    constexpr int NWARP = kQueueThreads / 32;
+    constexpr uint32_t NWARP = kQueueThreads / 32;
     const Args& A = Q.f;
     __shared__ uint32_t s_claim, s_tag;
-    __shared__ uint32_t wmax[2][NWARP][W];   // per-warp absmax partials, double-buffered by item
+    // absmax of each item of the claim by rank, folded in by the warps with shared atomics, and the
+    // count of warps done with the item: the last one publishes (no block-wide barrier per item)
+    __shared__ uint32_t s_max[kQueueBatch][W];
+    __shared__ uint32_t s_cnt[kQueueBatch];
     // the scales of the pass-2 chunk held: by rank (sq), and by row twice over, so that row k of a
     // slice with ring start rot reads entry k + rot
     __shared__ ScaleQ sq[W];
@@ -191,12 +194,13 @@ __global__ void __launch_bounds__(kQueueThreads, GQ_QUEUE_MIN_CTAS) k_queue(cons
         s_tag = *reinterpret_cast<volatile uint32_t*>(Q.ws + 2) + 1u;
         s_claim = atomicAdd(head, static_cast<uint32_t>(kQueueBatch));
     }
+    if (tid < kQueueBatch * W) s_max[tid / W][tid % W] = 0;
+    if (tid < kQueueBatch) s_cnt[tid] = 0;
     __syncthreads();
     const uint32_t tag = s_tag;
     const uint64_t wait_limit = g_wait_limit_ns;
     int64_t cached = -1;  // chunk whose scales the shared tables hold
     bool failed = false;
-    int parity = 0;
 
     for (;;) {
         const int64_t base = s_claim;
@@ -290,21 +294,30 @@ __global__ void __launch_bounds__(kQueueThreads, GQ_QUEUE_MIN_CTAS) k_queue(cons
 #pragma unroll
                     for (int k = 0; k < W; ++k) mx[k] = group_absmax<DT>(v[k], e0, full, g.slo, g.shi, mx[k]);
                 }
+                uint32_t mine = 0;
 #pragma unroll
                 for (int k = 0; k < W; ++k) {
                     const uint32_t m = __reduce_max_sync(0xffffffffu, mx[k]);
-                    if (lane == k) wmax[parity][warp][k] = m;
+                    if (lane == k) mine = m;
                 }
-                __syncthreads();
-                if (tid < W) {
-                    uint32_t m = 0;
-#pragma unroll
-                    for (int w2 = 0; w2 < NWARP; ++w2) m = max(m, wmax[parity][w2][tid]);
-                    // tag and value in one store: a reader never sees one without the other
-                    st_relaxed_gpu_u64(Q.slots + (static_cast<size_t>(j) * S + slice) * W + tid,
-                                       (static_cast<uint64_t>(tag) << 32) | m);
+                if (lane < W && mine != 0) atomicMax(&s_max[b][lane], mine);
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) {
+                    __threadfence_block();  // this warp's maxima before its count
+                    last = atomicAdd(&s_cnt[b], 1u) == NWARP - 1;
+                    if (last) __threadfence_block();  // every other warp's maxima before the reads below
                 }
-                parity ^= 1;
+                if (__shfl_sync(0xffffffffu, last, 0)) {
+                    if (lane < W) {
+                        const uint32_t m = s_max[b][lane];
+                        // tag and value in one store: a reader never sees one without the other
+                        st_relaxed_gpu_u64(Q.slots + (static_cast<size_t>(j) * S + slice) * W + lane,
+                                           (static_cast<uint64_t>(tag) << 32) | m);
+                        s_max[b][lane] = 0;  // for the next claim (past the claim barrier)
+                    }
+                    if (lane == 0) s_cnt[b] = 0;
+                }
             } else {
                 if (slice == 0 && tid < W) {
                     if (s_nonfinite[tid]) raise_error(kErrNonfinite);
