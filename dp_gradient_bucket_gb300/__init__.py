@@ -6,7 +6,7 @@ missing or fails to load, importing the binding raises.
 
 Functions keep the C names: gq_plan_buckets, gq_plan_chunks, gq_quantize,
 gq_reduce_dequant, gq_fused_allreduce_sim, gq_fused_workspace_bytes, gq_fused_allreduce_sim_ws,
-gq_get_error, gq_status_string.  Device
+gq_fused_allreduce_sim_static, gq_get_error, gq_status_string.  Device
 arguments are CUDA torch tensors (contiguous; their storage is used as is); `stream` is a
 torch.cuda.Stream, a raw cudaStream_t integer, or None for torch's current stream.
 """
@@ -26,6 +26,8 @@ GQ_ERR_TIMEOUT = 4
 GQ_ERR_UNSUPPORTED = 5
 GQ_WARN_NONFINITE = 6
 GQ_ERR_BAD_TABLE = 7
+GQ_ERR_TOO_LARGE = 8
+GQ_STATIC_SCRATCH_BYTES = 1 << 20
 
 GQ_F32, GQ_F16 = 0, 1
 GQ_ORDER_SEQ, GQ_ORDER_RING, GQ_ORDER_TREE = 0, 1, 2
@@ -52,6 +54,7 @@ def _load():
     L.gq_reduce_dequant.argtypes = [p, p, i32, sz, p, sz, i32, p, p]
     L.gq_fused_allreduce_sim.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p]
     L.gq_fused_allreduce_sim_ws.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p, sz, p]
+    L.gq_fused_allreduce_sim_static.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p]
     L.gq_fused_workspace_bytes.argtypes = [sz, i32]
     L.gq_fused_workspace_bytes.restype = sz
     L.gq_get_error.argtypes = [p]
@@ -60,7 +63,8 @@ def _load():
     L.gq_status_string.argtypes = [i32]
     L.gq_status_string.restype = ctypes.c_char_p
     for name in ("gq_plan_buckets", "gq_plan_chunks", "gq_quantize", "gq_reduce_dequant",
-                 "gq_fused_allreduce_sim", "gq_fused_allreduce_sim_ws", "gq_get_error"):
+                 "gq_fused_allreduce_sim", "gq_fused_allreduce_sim_ws", "gq_fused_allreduce_sim_static",
+                 "gq_get_error"):
         getattr(L, name).restype = i32
     return L
 
@@ -171,6 +175,17 @@ def gq_fused_allreduce_sim_ws(grads, W, rank_stride, d_offsets, num_chunks, loss
                                        _dptr(scales), _dptr(workspace), workspace.numel() * workspace.element_size(),
                                        _stream(stream))
     _check(st, "gq_fused_allreduce_sim_ws")
+
+
+def gq_fused_allreduce_sim_static(grads, W, rank_stride, d_offsets, num_chunks, loss_scale, order, out, codes=None,
+                                  scales=None, stream=None):
+    """gq_fused_allreduce_sim on the library's own static device scratch (no workspace, nothing
+    allocated); GQError(GQ_ERR_TOO_LARGE) when the table needs more than GQ_STATIC_SCRATCH_BYTES.
+    Calls that overlap on the device race on the one scratch array: keep them on one stream."""
+    st = lib.gq_fused_allreduce_sim_static(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
+                                           num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out),
+                                           _dptr(codes), _dptr(scales), _stream(stream))
+    _check(st, "gq_fused_allreduce_sim_static")
 
 
 def gq_get_error(stream=None):

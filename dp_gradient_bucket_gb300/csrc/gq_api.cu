@@ -4,6 +4,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 #include <vector>
 
 #include "gq.h"
@@ -236,6 +237,65 @@ gq_status gq_fused_allreduce_sim_ws(const void* d_grads, gq_dtype dt, int W, siz
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+}  // extern "C"
+
+// ----------------------------------------------------------------- gq_fused_allreduce_sim_static
+
+// The library's own scratch for the work queue, one per device (zero at module load; each call
+// clears the part it uses).
+static __device__ __align__(256) unsigned char g_static_scratch[GQ_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+struct StaticScratch {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    void* ptr = nullptr;
+};
+StaticScratch g_static_scratch_dev[64];
+
+}  // namespace
+
+extern "C" {
+
+gq_status gq_fused_allreduce_sim_static(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                        const int64_t* d_offsets, size_t num_chunks, float loss_scale,
+                                        gq_order order, float* d_out, int8_t* d_codes_opt, float* d_scales_opt,
+                                        gq_stream_t stream) {
+    // every check of gq_fused_allreduce_sim_ws that does not concern the workspace, first, so that
+    // an invalid call enqueues nothing
+    gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
+    if (st != GQ_OK) return st;
+    if (!d_out) return GQ_ERR_INVALID_ARG;
+    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (!aligned(d_out, 16) || (d_codes_opt && !aligned(d_codes_opt, 16)) ||
+        (d_scales_opt && !aligned(d_scales_opt, 4)))
+        return GQ_ERR_MISALIGNED;
+    const size_t gbytes = static_cast<size_t>(W) * rank_stride * elem_bytes_of(dt);
+    const size_t obytes = rank_stride * 4, cbytes = d_codes_opt ? static_cast<size_t>(W) * rank_stride : 0,
+                 sbytes = d_scales_opt ? static_cast<size_t>(W) * num_chunks * 4 : 0;
+    const void* bufs[4] = {d_grads, d_out, d_codes_opt, d_scales_opt};
+    const size_t sizes[4] = {gbytes, obytes, cbytes, sbytes};
+    for (int x = 0; x < 4; ++x)
+        for (int y = x + 1; y < 4; ++y)
+            if (overlaps(bufs[x], sizes[x], bufs[y], sizes[y])) return GQ_ERR_INVALID_ARG;
+    const size_t need = gq_fused_workspace_bytes(num_chunks, W);
+    if (need > GQ_STATIC_SCRATCH_BYTES) return GQ_ERR_TOO_LARGE;
+
+    // per-device setup: the array's device address
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GQ_ERR_CUDA;
+    StaticScratch& sc = g_static_scratch_dev[dev];
+    std::call_once(sc.once, [&] { sc.err = cudaGetSymbolAddress(&sc.ptr, g_static_scratch); });
+    if (sc.err != cudaSuccess || sc.ptr == nullptr) return GQ_ERR_CUDA;
+
+    // the scratch must start at zero: clear what this call uses, in stream order
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(sc.ptr, 0, need, s) != cudaSuccess) return GQ_ERR_CUDA;
+    return gq_fused_allreduce_sim_ws(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale, order, d_out,
+                                     d_codes_opt, d_scales_opt, sc.ptr, need, stream);
+}
+
 gq_status gq_get_error(gq_stream_t stream) {
     unsigned w = 0;
     const cudaError_t e = gq::read_and_clear_error_word(&w, reinterpret_cast<cudaStream_t>(stream));
@@ -261,6 +321,7 @@ const char* gq_status_string(gq_status s) {
         case GQ_ERR_UNSUPPORTED: return "GQ_ERR_UNSUPPORTED: device cannot run this kernel";
         case GQ_WARN_NONFINITE: return "GQ_WARN_NONFINITE: an input value was Inf or NaN";
         case GQ_ERR_BAD_TABLE: return "GQ_ERR_BAD_TABLE: a chunk table broke its rules";
+        case GQ_ERR_TOO_LARGE: return "GQ_ERR_TOO_LARGE: the problem needs more than the static scratch array";
     }
     return "unknown gq_status";
 }

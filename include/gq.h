@@ -64,7 +64,9 @@ typedef enum {
     GQ_ERR_TIMEOUT = 4,     /* a device-side bounded wait gave up (gq_get_error only)  */
     GQ_ERR_UNSUPPORTED = 5, /* the device cannot run the kernel (not sm_103, no clusters) */
     GQ_WARN_NONFINITE = 6,  /* an input value was Inf or NaN (gq_get_error only)       */
-    GQ_ERR_BAD_TABLE = 7    /* a chunk table broke the rules above (gq_get_error only) */
+    GQ_ERR_BAD_TABLE = 7,   /* a chunk table broke the rules above (gq_get_error only) */
+    GQ_ERR_TOO_LARGE = 8    /* the problem needs more scratch than the library's static array
+                               (gq_fused_allreduce_sim_static only)                     */
 } gq_status;
 
 typedef enum { GQ_F32 = 0, GQ_F16 = 1 } gq_dtype;
@@ -170,6 +172,31 @@ gq_status gq_fused_allreduce_sim_ws(const void* d_grads, gq_dtype dt, int W, siz
                                     gq_order order, float* d_out, int8_t* d_codes_opt,
                                     float* d_scales_opt, void* d_workspace, size_t workspace_bytes,
                                     gq_stream_t stream);
+
+/* Bytes of the library's own device scratch array used by gq_fused_allreduce_sim_static: 1 MiB,
+ * enough for chunk tables of up to 511 chunks at W = 8 (buckets of up to 64 MiB of fp32, or
+ * 128 MiB of fp16, per rank under dynamic_chunk). */
+#define GQ_STATIC_SCRATCH_BYTES ((size_t)1 << 20)
+
+/* gq_fused_allreduce_sim_ws with no caller workspace, allocating nothing: the work queue's scratch
+ * is a file-scope device array of GQ_STATIC_SCRATCH_BYTES inside the library.  The method's
+ * description (the "pipelined HCCL AllReduce" article) has no counterpart to this call; it
+ * exists for callers that can neither allocate nor own device memory for the step.
+ *   - Arguments, results (bit for bit) and errors as gq_fused_allreduce_sim, plus
+ *     GQ_ERR_TOO_LARGE, with nothing enqueued, when gq_fused_workspace_bytes(num_chunks, W)
+ *     exceeds GQ_STATIC_SCRATCH_BYTES.
+ *   - The first call on a device looks up the array's address (cudaGetSymbolAddress) and may
+ *     return GQ_ERR_CUDA if that fails; make that first call before any stream capture.
+ *   - Each call clears the part of the array it uses (cudaMemsetAsync on `stream`, so the
+ *     scratch starts at zero whatever an earlier call left) and launches the kernel; no memory
+ *     is allocated or freed, by the library or any library it calls.
+ *   - There is one array per device: calls that overlap on the device (on different streams,
+ *     or from different host threads without ordering) race on it and give wrong results.
+ *     Issue them on one stream. */
+gq_status gq_fused_allreduce_sim_static(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                        const int64_t* d_offsets, size_t num_chunks, float loss_scale,
+                                        gq_order order, float* d_out, int8_t* d_codes_opt,
+                                        float* d_scales_opt, gq_stream_t stream);
 
 /* Waits for `stream`, then reads and clears the current device's error word.  Returns
  * GQ_OK, or the most serious recorded condition: GQ_ERR_TIMEOUT, then GQ_ERR_BAD_TABLE,

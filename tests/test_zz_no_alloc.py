@@ -1,0 +1,75 @@
+"""gq_fused_allreduce_sim_static: the fused path on the library's own static device scratch.
+
+Collected last (file name), so it runs both after every other test and, run on its own, in a
+fresh process whose first call does the per-device setup.  Each GPU test calls the new entry
+point twice in a row through the C ABI and compares every output bit with gq_fused_allreduce_sim
+on the same inputs.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import dp_gradient_bucket_gb300 as gq
+import workloads as wl
+import _gpu as H
+
+
+def _outputs(W, stride, nc, n, dev):
+    out = torch.full((max(n, 4),), float("nan"), dtype=torch.float32, device=dev)
+    codes = torch.full((W * stride,), -91, dtype=torch.int8, device=dev)
+    scales = torch.full((W * nc,), float("nan"), dtype=torch.float32, device=dev)
+    return out, codes, scales
+
+
+def _compare_with_fused(host, W, stride, buckets, order, loss_scale):
+    dev = torch.device("cuda:0")
+    grads = torch.from_numpy(host).to(dev)
+    nc, d_off = H.plan_device(buckets, host.dtype.itemsize, dev)
+    n = int(d_off[-1].item())
+    want = _outputs(W, stride, nc, n, dev)
+    gq.gq_fused_allreduce_sim(grads, W, stride, d_off, nc, loss_scale, order, *want)
+    assert gq.gq_get_error() == gq.GQ_OK
+    for call in range(2):
+        got = _outputs(W, stride, nc, n, dev)
+        gq.gq_fused_allreduce_sim_static(grads, W, stride, d_off, nc, loss_scale, order, *got)
+        assert gq.gq_get_error() == gq.GQ_OK
+        for name, g, w in zip(("output", "codes", "scales"), got, want):
+            gb = g.cpu().numpy().view(np.uint8)
+            wb = w.cpu().numpy().view(np.uint8)
+            assert np.array_equal(gb, wb), "call %d: %s differs" % (call, name)
+
+
+@pytest.mark.gpu
+def test_static_scratch_matches_fused_25mib_ring():
+    W, n = 8, 6553600  # the 25 MiB bucket: 200 chunks, 409,616 bytes of scratch
+    host, stride = wl.rows(2, W, n)
+    _compare_with_fused(host, W, stride, [n], "ring", 1.0)
+
+
+@pytest.mark.gpu
+def test_static_scratch_matches_fused_fp16_tree_and_ragged_buckets():
+    W = 8
+    buckets = [5, 0, 65535, 131075, 3]
+    n = sum(buckets)
+    stride = gq.row_stride(n, 2)
+    host = np.zeros(W * stride, dtype=np.float16)
+    for r in range(W):
+        wl.fill(4, r, 0, n, host[r * stride:r * stride + n])
+    _compare_with_fused(host, W, stride, buckets, "tree", 65536.0)
+    _compare_with_fused(host, W, stride, buckets, "seq", 3.0)
+
+
+def test_static_scratch_rejects_tables_over_the_limit():
+    """No GPU needed: the size check comes before any CUDA call, and nothing is enqueued."""
+    W = 8
+    most = (gq.GQ_STATIC_SCRATCH_BYTES - 16) // (32 * W * 8)  # 511 chunks fit
+    assert gq.gq_fused_workspace_bytes(most, W) <= gq.GQ_STATIC_SCRATCH_BYTES
+    assert gq.gq_fused_workspace_bytes(most + 1, W) > gq.GQ_STATIC_SCRATCH_BYTES
+    p = ctypes.c_void_p
+    fake = [p(0x100000), p(0x900000000), p(0x200000)]  # grads, out, offsets: aligned, never touched
+    st = gq.lib.gq_fused_allreduce_sim_static(fake[0], gq.GQ_F32, W, 1 << 16, fake[2], most + 1, 1.0,
+                                              gq.GQ_ORDER_RING, fake[1], None, None, None)
+    assert st == gq.GQ_ERR_TOO_LARGE
+    assert "static scratch" in gq.gq_status_string(st)
