@@ -6,7 +6,8 @@ missing or fails to load, importing the binding raises.
 
 Functions keep the C names: gq_plan_buckets, gq_plan_chunks, gq_quantize,
 gq_reduce_dequant, gq_fused_allreduce_sim, gq_fused_workspace_bytes, gq_fused_allreduce_sim_ws,
-gq_fused_allreduce_sim_static, gq_get_error, gq_status_string.  Device
+gq_fused_allreduce_sim_static, gq_fused_allreduce_sim_amp, gq_amp_update_scale, gq_get_error,
+gq_status_string.  Device
 arguments are CUDA torch tensors (contiguous; their storage is used as is); `stream` is a
 torch.cuda.Stream, a raw cudaStream_t integer, or None for torch's current stream.
 """
@@ -55,6 +56,8 @@ def _load():
     L.gq_fused_allreduce_sim.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p]
     L.gq_fused_allreduce_sim_ws.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p, sz, p]
     L.gq_fused_allreduce_sim_static.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p]
+    L.gq_fused_allreduce_sim_amp.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p, p]
+    L.gq_amp_update_scale.argtypes = [p, p, p, ctypes.c_float, ctypes.c_float, i32, p]
     L.gq_fused_workspace_bytes.argtypes = [sz, i32]
     L.gq_fused_workspace_bytes.restype = sz
     L.gq_get_error.argtypes = [p]
@@ -64,7 +67,7 @@ def _load():
     L.gq_status_string.restype = ctypes.c_char_p
     for name in ("gq_plan_buckets", "gq_plan_chunks", "gq_quantize", "gq_reduce_dequant",
                  "gq_fused_allreduce_sim", "gq_fused_allreduce_sim_ws", "gq_fused_allreduce_sim_static",
-                 "gq_get_error"):
+                 "gq_fused_allreduce_sim_amp", "gq_amp_update_scale", "gq_get_error"):
         getattr(L, name).restype = i32
     return L
 
@@ -186,6 +189,25 @@ def gq_fused_allreduce_sim_static(grads, W, rank_stride, d_offsets, num_chunks, 
                                            num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out),
                                            _dptr(codes), _dptr(scales), _stream(stream))
     _check(st, "gq_fused_allreduce_sim_static")
+
+
+def gq_fused_allreduce_sim_amp(grads, W, rank_stride, d_offsets, num_chunks, loss_scale, order, out, found_inf,
+                               codes=None, scales=None, stream=None):
+    """gq_fused_allreduce_sim that also sets the device float `found_inf` to 1.0 when an input value
+    is Inf or NaN (or overflows when unscaled), leaving it alone otherwise."""
+    st = lib.gq_fused_allreduce_sim_amp(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
+                                        num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out), _dptr(codes),
+                                        _dptr(scales), _dptr(found_inf), _stream(stream))
+    _check(st, "gq_fused_allreduce_sim_amp")
+
+
+def gq_amp_update_scale(scale, growth_tracker, found_inf, growth_factor=2.0, backoff_factor=0.5,
+                        growth_interval=2000, stream=None):
+    """GradScaler's loss-scale update on the device: scale (float32), growth_tracker (int32) and
+    found_inf (float32) are one-element CUDA tensors."""
+    st = lib.gq_amp_update_scale(_dptr(scale), _dptr(growth_tracker), _dptr(found_inf), growth_factor,
+                                 backoff_factor, growth_interval, _stream(stream))
+    _check(st, "gq_amp_update_scale")
 
 
 def gq_get_error(stream=None):

@@ -74,6 +74,7 @@ gq::QuantArgs quant_args(const void* d_grads, gq_dtype dt, int W, size_t rank_st
     a.num_chunks = static_cast<int64_t>(num_chunks);
     a.inv = static_cast<float>(1.0 / static_cast<double>(loss_scale));
     a.scaled = a.inv != 1.0f;
+    a.found_inf = nullptr;
     return a;
 }
 
@@ -204,6 +205,42 @@ gq_status gq_fused_allreduce_sim(const void* d_grads, gq_dtype dt, int W, size_t
     const gq::QuantArgs a = quant_args(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
     return from_cuda(gq::launch_fused(a, static_cast<int>(order), d_out, d_codes_opt, d_scales_opt,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gq_status gq_fused_allreduce_sim_amp(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                     const int64_t* d_offsets, size_t num_chunks, float loss_scale, gq_order order,
+                                     float* d_out, int8_t* d_codes_opt, float* d_scales_opt, float* d_found_inf,
+                                     gq_stream_t stream) {
+    gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
+    if (st != GQ_OK) return st;
+    if (!d_out || !d_found_inf) return GQ_ERR_INVALID_ARG;
+    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (!aligned(d_out, 16) || (d_codes_opt && !aligned(d_codes_opt, 16)) ||
+        (d_scales_opt && !aligned(d_scales_opt, 4)) || !aligned(d_found_inf, 4))
+        return GQ_ERR_MISALIGNED;
+    const size_t gbytes = static_cast<size_t>(W) * rank_stride * elem_bytes_of(dt);
+    const size_t obytes = rank_stride * 4, cbytes = d_codes_opt ? static_cast<size_t>(W) * rank_stride : 0,
+                 sbytes = d_scales_opt ? static_cast<size_t>(W) * num_chunks * 4 : 0;
+    const void* bufs[5] = {d_grads, d_out, d_codes_opt, d_scales_opt, d_found_inf};
+    const size_t sizes[5] = {gbytes, obytes, cbytes, sbytes, 4};
+    for (int x = 0; x < 5; ++x)
+        for (int y = x + 1; y < 5; ++y)
+            if (overlaps(bufs[x], sizes[x], bufs[y], sizes[y])) return GQ_ERR_INVALID_ARG;
+    gq::QuantArgs a = quant_args(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
+    a.found_inf = d_found_inf;
+    return from_cuda(gq::launch_fused(a, static_cast<int>(order), d_out, d_codes_opt, d_scales_opt,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+gq_status gq_amp_update_scale(float* d_scale, int32_t* d_growth_tracker, const float* d_found_inf,
+                              float growth_factor, float backoff_factor, int growth_interval, gq_stream_t stream) {
+    if (!d_scale || !d_growth_tracker || !d_found_inf) return GQ_ERR_INVALID_ARG;
+    if (!aligned(d_scale, 4) || !aligned(d_growth_tracker, 4) || !aligned(d_found_inf, 4)) return GQ_ERR_MISALIGNED;
+    if (growth_interval < 1 || !(growth_factor > 0.0f) || !(backoff_factor > 0.0f) || !std::isfinite(growth_factor) ||
+        !std::isfinite(backoff_factor))
+        return GQ_ERR_INVALID_ARG;
+    return from_cuda(gq::launch_amp_update(d_scale, d_growth_tracker, d_found_inf, growth_factor, backoff_factor,
+                                           growth_interval, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t gq_fused_workspace_bytes(size_t num_chunks, int W) {

@@ -349,7 +349,10 @@ __device__ __forceinline__ bool exchange_scales(const Args& A, int W, uint32_t P
         sq[tid] = s;
         not_subnormal = s.mode != 2;
         if (crank == 0) {
-            if (nonfinite) raise_error(kErrNonfinite);
+            if (nonfinite) {
+                raise_error(kErrNonfinite);
+                if (A.q.found_inf) *A.q.found_inf = 1.0f;
+            }
             if (A.scales) A.scales[static_cast<int64_t>(tid) * A.q.num_chunks + j] = s.s;
         }
     }

@@ -36,9 +36,14 @@ struct QuantArgs {
     int64_t num_chunks;
     float inv;   // (float)(1 / loss_scale)
     int scaled;  // inv != 1
+    float* found_inf;  // may be null: set to 1.0f when an unscaled input value is Inf or NaN
 };
 
 cudaError_t launch_quantize(const QuantArgs& a, int8_t* codes, float* scales, cudaStream_t stream);
+
+// GradScaler's scale update on the device (one thread): see gq_amp_update_scale.
+cudaError_t launch_amp_update(float* scale, int32_t* growth_tracker, const float* found_inf, float growth_factor,
+                              float backoff_factor, int growth_interval, cudaStream_t stream);
 
 cudaError_t launch_reduce(const int8_t* codes, const float* scales, int W, int64_t rank_stride,
                           const int64_t* offsets, int64_t num_chunks, int order, float* out,

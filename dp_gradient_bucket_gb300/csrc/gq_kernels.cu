@@ -142,7 +142,10 @@ __global__ void __launch_bounds__(kThreads) k_quantize(const QuantArgs a, int8_t
     const ScaleQ sq = make_scale(m);
     if (threadIdx.x == 0) {
         scales[static_cast<int64_t>(r) * a.num_chunks + j] = sq.s;
-        if (nonfinite) raise_error(kErrNonfinite);
+        if (nonfinite) {
+            raise_error(kErrNonfinite);
+            if (a.found_inf) *a.found_inf = 1.0f;
+        }
     }
 
     int8_t* crow = codes + static_cast<int64_t>(r) * a.rank_stride;
@@ -307,6 +310,36 @@ cudaError_t launch_fused_ws(const QuantArgs& a, int order, float* out, int8_t* c
                   : launch_queue_f16(a, order, out, codes, scales, workspace, workspace_bytes, stream, &launched);
     if (launched || e != cudaSuccess) return e;
     return launch_fused(a, order, out, codes, scales, stream);
+}
+
+// ===================================================================== GradScaler update
+
+// The dynamic loss-scale update of torch.cuda.amp.GradScaler.update (the step after the found-inf
+// check): on an overflow the scale is multiplied by backoff_factor and the growth count restarts;
+// after growth_interval clean steps in a row it is multiplied by growth_factor (kept only if the
+// product is finite) and the count restarts.  One thread: the whole state is two words.
+__global__ void k_amp_update(float* scale, int32_t* growth_tracker, const float* found_inf, float growth_factor,
+                             float backoff_factor, int growth_interval) {
+    if (*found_inf != 0.0f) {
+        *scale = __fmul_rn(*scale, backoff_factor);
+        *growth_tracker = 0;
+        return;
+    }
+    const int32_t successful = *growth_tracker + 1;
+    if (successful == growth_interval) {
+        const float grown = __fmul_rn(*scale, growth_factor);
+        if (isfinite(grown)) *scale = grown;
+        *growth_tracker = 0;
+    } else {
+        *growth_tracker = successful;
+    }
+}
+
+cudaError_t launch_amp_update(float* scale, int32_t* growth_tracker, const float* found_inf, float growth_factor,
+                              float backoff_factor, int growth_interval, cudaStream_t stream) {
+    k_amp_update<<<1, 1, 0, stream>>>(scale, growth_tracker, found_inf, growth_factor, backoff_factor,
+                                      growth_interval);
+    return cudaGetLastError();
 }
 
 // ===================================================================== error word

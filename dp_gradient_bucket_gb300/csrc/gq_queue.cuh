@@ -320,7 +320,10 @@ __global__ void __launch_bounds__(kQueueThreads, GQ_QUEUE_MIN_CTAS) k_queue(cons
                 }
             } else {
                 if (slice == 0 && tid < W) {
-                    if (s_nonfinite[tid]) raise_error(kErrNonfinite);
+                    if (s_nonfinite[tid]) {
+                        raise_error(kErrNonfinite);
+                        if (A.q.found_inf) *A.q.found_inf = 1.0f;
+                    }
                     if (A.scales) A.scales[static_cast<int64_t>(tid) * n + j] = sq[tid].s;
                 }
                 const int rot = g.rot;

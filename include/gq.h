@@ -148,6 +148,31 @@ gq_status gq_fused_allreduce_sim(const void* d_grads, gq_dtype dt, int W, size_t
                                  gq_order order, float* d_out, int8_t* d_codes_opt,
                                  float* d_scales_opt, gq_stream_t stream);
 
+/* gq_fused_allreduce_sim for a mixed-precision step (the "pipelined HCCL AllReduce" article, §6.1:
+ * unscale before quantising; torch.cuda.amp semantics): same arguments, results and errors, plus
+ *   d_found_inf  device float, 4-byte aligned, not overlapping the other buffers: set to 1.0f when
+ *                any input value of any rank is Inf or NaN, or overflows when unscaled; left as it
+ *                is otherwise (zero it before the step, as GradScaler does).  The step can then be
+ *                skipped on the device (see gq_amp_update_scale) with no host synchronisation.
+ * GQ_ERR_INVALID_ARG if d_found_inf is NULL. */
+gq_status gq_fused_allreduce_sim_amp(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                     const int64_t* d_offsets, size_t num_chunks, float loss_scale,
+                                     gq_order order, float* d_out, int8_t* d_codes_opt,
+                                     float* d_scales_opt, float* d_found_inf, gq_stream_t stream);
+
+/* The dynamic loss-scale update that follows the found-inf check (torch.cuda.amp.GradScaler.update),
+ * on the device, one launch on `stream`:
+ *   *d_found_inf != 0:  *d_scale = fl(*d_scale * backoff_factor); *d_growth_tracker = 0
+ *   else:               t = *d_growth_tracker + 1;
+ *                       t == growth_interval: g = fl(*d_scale * growth_factor); if g is finite,
+ *                                             *d_scale = g; *d_growth_tracker = 0
+ *                       otherwise:            *d_growth_tracker = t
+ * All three pointers are device words (4-byte aligned).  GQ_ERR_INVALID_ARG for a NULL pointer,
+ * growth_interval < 1, or a factor that is not a finite positive number. */
+gq_status gq_amp_update_scale(float* d_scale, int32_t* d_growth_tracker, const float* d_found_inf,
+                              float growth_factor, float backoff_factor, int growth_interval,
+                              gq_stream_t stream);
+
 /* Bytes of device workspace gq_fused_allreduce_sim_ws needs for a chunk table of num_chunks chunks
  * and W ranks: 16 + num_chunks * 32 * W * 8 (a 16-byte header and one 8-byte word per chunk,
  * slice and rank; 2 KiB per chunk at W = 8, 0.2% of the 1 MiB of fp32 gradients it covers). */

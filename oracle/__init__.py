@@ -34,6 +34,8 @@ def lib():
         L.oracle_quantize.restype = i64
         L.oracle_reduce.argtypes = [p, p, ctypes.c_int, i64, p, i64, ctypes.c_int, p]
         L.oracle_reduce.restype = None
+        L.oracle_amp_update_scale.argtypes = [p, p, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_int32]
+        L.oracle_amp_update_scale.restype = None
         L.oracle_half_to_float.argtypes = [ctypes.c_uint16]
         L.oracle_half_to_float.restype = ctypes.c_float
         _lib = L
@@ -114,3 +116,12 @@ def fused(grads, W, rank_stride, offsets, order, loss_scale=1.0):
 
 def half_to_float(bits):
     return float(lib().oracle_half_to_float(int(bits)))
+
+
+def amp_update_scale(scale, tracker, found_inf, growth=2.0, backoff=0.5, interval=2000):
+    """One GradScaler update step; returns (scale float32, tracker int)."""
+    sc = np.array([scale], dtype=np.float32)
+    tr = np.array([tracker], dtype=np.int32)
+    lib().oracle_amp_update_scale(_ptr(sc), _ptr(tr), float(np.float32(found_inf)), float(growth), float(backoff),
+                                  int(interval))
+    return sc[0], int(tr[0])

@@ -182,4 +182,22 @@ void oracle_reduce(const int8_t* codes, const float* scales, int W, int64_t rank
     }
 }
 
+void oracle_amp_update_scale(float* scale, int32_t* tracker, float found_inf, float growth, float backoff,
+                             int32_t interval) {
+    if (found_inf != 0.0f) {  // true for NaN as well
+        const float backed = *scale * backoff;
+        *scale = backed;
+        *tracker = 0;
+        return;
+    }
+    const int32_t t = *tracker + 1;
+    if (t == interval) {
+        const float grown = *scale * growth;
+        if (std::isfinite(grown)) *scale = grown;
+        *tracker = 0;
+    } else {
+        *tracker = t;
+    }
+}
+
 }  // extern "C"

@@ -82,6 +82,14 @@ int64_t oracle_quantize(const void* grads, int dt, int W, int64_t rank_stride,
 void oracle_reduce(const int8_t* codes, const float* scales, int W, int64_t rank_stride,
                    const int64_t* offsets, int64_t num_chunks, int order, float* out);
 
+/* One step of the dynamic loss-scale update that follows the found-inf check in a mixed-precision
+ * step ([HCCL-PIPE] §6.1 mixed precision; torch.cuda.amp.GradScaler.update semantics):
+ *   found_inf != 0 (NaN counts as set): scale = (float)(scale * backoff), tracker = 0
+ *   otherwise: t = tracker + 1; if t == interval: g = (float)(scale * growth), scale = g only
+ *              if g is finite, tracker = 0; else tracker = t. */
+void oracle_amp_update_scale(float* scale, int32_t* tracker, float found_inf, float growth, float backoff,
+                             int32_t interval);
+
 /* Exact binary16 -> binary32 decode (used by the oracle's F16 path; exported so the
  * decode can be pinned on its own). */
 float oracle_half_to_float(uint16_t h);

@@ -23,6 +23,7 @@ import _golden as G
 import test_oracle_exact as TE
 import test_oracle_golden as TG
 import test_oracle_plan as TP
+import test_oracle_amp as TA
 
 MUTANTS = {
     "scale_divisor_128": ("m / 127.0f", "m / 128.0f"),
@@ -51,6 +52,10 @@ MUTANTS = {
     "half_exponent_bias": ("e - 25", "e - 24"),
     "half_subnormal_scale": ("static_cast<double>(f), -24", "static_cast<double>(f), -25"),
     "zero_scale_not_special": ("if (finite && s != 0.0f) {", "if (finite) {"),
+    "amp_overflow_keeps_count": ("        *tracker = 0;\n        return;", "        return;"),
+    "amp_growth_unguarded": ("if (std::isfinite(grown)) *scale = grown;", "*scale = grown;"),
+    "amp_interval_late": ("if (t == interval) {", "if (t > interval) {"),
+    "amp_nan_not_overflow": ("if (found_inf != 0.0f) {", "if (found_inf > 0.0f) {"),
 }
 
 
@@ -64,6 +69,9 @@ def _battery(orc):
         ("multi_bucket", lambda: TP.test_plan_multi_bucket_table(orc)),
         ("mean_div", lambda: TE.test_mean_division_nonpower_of_two(orc)),
         ("half_decode", lambda: TE.test_half_decode_all_patterns(orc)),
+        ("amp_golden", TA.test_update_sequence_golden),
+        ("amp_overflow_guard", TA.test_growth_that_overflows_keeps_the_scale),
+        ("amp_closed_form", TA.test_closed_form_over_long_runs),
     ]
     for name, case in G.keyed_cases("quantize_cases.txt"):
         checks.append(("quantize:" + name, lambda c=case, n=name: TG.test_quantize_cases(orc, n, c)))

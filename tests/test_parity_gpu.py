@@ -224,7 +224,7 @@ def test_rank_counts(W):
     for r in range(W):
         wl.fill(1, r, 0, n, host[r * stride:r * stride + n])
     for order, oorder in ORDERS:
-        for mode in ("fused", "two_kernel"):
+        for mode in ("fused", "fused_ws", "two_kernel"):
             out, codes, scales, off, st = H.run(host, W, stride, [n], order, mode=mode)
             assert st == gq.GQ_OK
             H.compare_full(host, W, stride, off, oorder, 1.0, out, codes, scales)
@@ -464,3 +464,65 @@ def test_ws_epoch_wrap_clears_words():
             assert int(ws[4:].abs().sum().item()) == 0  # every word cleared
         else:
             assert int(ws[2].item()) == k
+
+
+# ------------------------------------------------------------------ mixed precision: found-inf and scale update
+
+@pytest.mark.parametrize("W", [4, 8])
+def test_amp_found_inf_flag(W):
+    """The flag is set exactly when the oracle counts a non-finite (rank, chunk); the outputs equal
+    those of gq_fused_allreduce_sim bit for bit."""
+    n = 300000
+    stride = gq.row_stride(n, 4)
+    host = np.zeros(W * stride, dtype=np.float32)
+    for r in range(W):
+        wl.fill(1, r, 0, n, host[r * stride:r * stride + n])
+    dev = torch.device("cuda:0")
+    off = oracle.plan_chunks([n], 4)
+    for case in ("finite", "inf", "nan", "overflow"):
+        h = host.copy()
+        ls = 1.0
+        if case == "inf":
+            h[(W - 1) * stride + 123456] = np.inf
+        elif case == "nan":
+            h[5] = np.nan
+        elif case == "overflow":
+            h[stride + 7] = np.float32(3e38)
+            ls = 0.5  # unscaling doubles it past the binary32 range
+        _, _, nf = oracle.quantize(h, W, stride, off, loss_scale=ls)
+        grads = torch.from_numpy(h).to(dev)
+        d_off = torch.from_numpy(off).to(dev)
+        nc = len(off) - 1
+        found = torch.zeros(1, dtype=torch.float32, device=dev)
+        out_a = torch.empty(stride, dtype=torch.float32, device=dev)
+        out_b = torch.empty(stride, dtype=torch.float32, device=dev)
+        gq.gq_fused_allreduce_sim_amp(grads, W, stride, d_off, nc, ls, "ring", out_a, found)
+        st = gq.gq_get_error()
+        gq.gq_fused_allreduce_sim(grads, W, stride, d_off, nc, ls, "ring", out_b)
+        gq.gq_get_error()
+        assert float(found.item()) == (1.0 if nf > 0 else 0.0), case
+        assert st == (gq.GQ_WARN_NONFINITE if nf > 0 else gq.GQ_OK), case
+        if nf == 0:
+            H.assert_bits_equal(out_a.cpu().numpy()[:n], out_b.cpu().numpy()[:n], "amp vs plain")
+            want = oracle.fused(h, W, stride, off, oracle.RING, ls)[0]
+            H.assert_bits_equal(out_a.cpu().numpy()[:n], want, "amp vs oracle")
+
+
+def test_amp_update_scale_matches_oracle():
+    """A long random sequence of found-inf values (0, 1, NaN) through the device update and the
+    oracle, with factors whose products round, and with an interval small enough to grow often."""
+    dev = torch.device("cuda:0")
+    rng = np.random.default_rng(11)
+    for growth, backoff, interval, s0 in ((2.0, 0.5, 3, 65536.0), (1.1, 0.3, 2, 3.0), (2.0, 0.5, 1, 2.0 ** 120)):
+        scale = torch.tensor([s0], dtype=torch.float32, device=dev)
+        tracker = torch.zeros(1, dtype=torch.int32, device=dev)
+        found = torch.zeros(1, dtype=torch.float32, device=dev)
+        ws, wt = np.float32(s0), 0
+        for step in range(400):
+            f = [0.0, 0.0, 0.0, 1.0, float("nan")][rng.integers(0, 5)]
+            found.fill_(f)
+            gq.gq_amp_update_scale(scale, tracker, found, growth, backoff, interval)
+            ws, wt = oracle.amp_update_scale(ws, wt, f, growth, backoff, interval)
+            got = scale.cpu().numpy()
+            assert got.view(np.uint32)[0] == np.array([ws], dtype=np.float32).view(np.uint32)[0], (step, got, ws)
+            assert int(tracker.item()) == wt, step
