@@ -47,8 +47,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length (cpu_baseline)")
-    p.add_argument("--entry", default="plain", choices=["ws", "plain"],
-                   help="ws: gq_fused_allreduce_sim_ws (work-queue kernel); plain: gq_fused_allreduce_sim")
+    p.add_argument("--entry", default="plain", choices=["ws", "plain", "pipe"],
+                   help="ws: gq_fused_allreduce_sim_ws (work-queue kernel); plain: gq_fused_allreduce_sim; "
+                        "pipe: gq_fused_allreduce_sim_pipelined")
     return p.parse_args()
 
 
@@ -233,9 +234,14 @@ def run_gq(args):
     stream = torch.cuda.current_stream(dev)
     # the caller-owned workspace of the work-queue entry point: zeroed once, left zeroed by every call
     wspace = torch.zeros(gq.gq_fused_workspace_bytes(nc, W) // 4, dtype=torch.int32, device=dev)
+    # the pipelined entry point's workspace (counters, scale words, L2-resident codes)
+    pspace = (torch.zeros(gq.gq_pipelined_workspace_bytes(W, stride, nc), dtype=torch.uint8, device=dev)
+              if args.entry == "pipe" else None)
 
     def fused(inp):
-        if args.entry == "ws":
+        if args.entry == "pipe":
+            gq.gq_fused_allreduce_sim_pipelined(inp, W, stride, offsets, nc, 1.0, "ring", out, pspace, stream=stream)
+        elif args.entry == "ws":
             gq.gq_fused_allreduce_sim_ws(inp, W, stride, offsets, nc, 1.0, "ring", out, wspace, stream=stream)
         else:
             gq.gq_fused_allreduce_sim(inp, W, stride, offsets, nc, 1.0, "ring", out, stream=stream)
@@ -318,7 +324,7 @@ def run_gq(args):
     peak = float(peaks["hbm_gbs"])
     alg_bytes = IN_BYTES + OUT_BYTES
     achieved = alg_bytes / (kern_avg_ms * 1e-3) / 1e9
-    kernel = "k_queue<f32>" if args.entry == "ws" else "k_fused<f32, W=8>"
+    kernel = {"ws": "k_queue<f32>", "pipe": "k_pipe<f32>"}.get(args.entry, "k_fused<f32, W=8>")
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "fused_traffic.json")
     if os.path.exists(tpath):
@@ -340,8 +346,9 @@ def run_gq(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "order": "ring", "chunks": nc, "input_bytes_per_step": IN_BYTES,
                    "l2": "%d rotating input sets of %d MB (> 129 MB L2)" % (INPUT_SETS, IN_BYTES // 10 ** 6),
-                   "step": "gq_plan_chunks + " + ("gq_fused_allreduce_sim_ws" if args.entry == "ws"
-                                                  else "gq_fused_allreduce_sim")},
+                   "step": "gq_plan_chunks + " + {"ws": "gq_fused_allreduce_sim_ws",
+                                                  "pipe": "gq_fused_allreduce_sim_pipelined"}.get(
+                                                      args.entry, "gq_fused_allreduce_sim")},
         "hbm_peak_fraction": value / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "kernel": kernel, "kernel_avg_us": kern_avg_ms * 1e3,

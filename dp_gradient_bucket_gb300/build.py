@@ -15,9 +15,9 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libgq.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["gq_queue_f16.cu", "gq_queue_f32.cu", "gq_fused_f16.cu", "gq_fused_f32.cu",
+SOURCES = ["gq_pipe_f16.cu", "gq_pipe_f32.cu", "gq_queue_f16.cu", "gq_queue_f32.cu", "gq_fused_f16.cu", "gq_fused_f32.cu",
            "gq_kernels.cu", "gq_api.cu"]
-HEADERS = ["gq_device.cuh", "gq_internal.h", "gq_fused.cuh", "gq_queue.cuh"]
+HEADERS = ["gq_device.cuh", "gq_internal.h", "gq_fused.cuh", "gq_queue.cuh", "gq_pipe.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-Wall", "-I" + os.path.join(ROOT, "include")]

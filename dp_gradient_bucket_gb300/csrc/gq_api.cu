@@ -274,6 +274,42 @@ gq_status gq_fused_allreduce_sim_ws(const void* d_grads, gq_dtype dt, int W, siz
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t gq_pipelined_workspace_bytes(int W, size_t rank_stride, size_t num_chunks) {
+    if (W < 1) W = 1;
+    return gq::pipe_workspace_bytes(W, static_cast<int64_t>(rank_stride), static_cast<int64_t>(num_chunks));
+}
+
+gq_status gq_fused_allreduce_sim_pipelined(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                           const int64_t* d_offsets, size_t num_chunks, float loss_scale,
+                                           gq_order order, float* d_out, int8_t* d_codes_opt, float* d_scales_opt,
+                                           float* d_found_inf_opt, void* d_workspace, size_t workspace_bytes,
+                                           gq_stream_t stream) {
+    gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
+    if (st != GQ_OK) return st;
+    if (!d_out || !d_workspace) return GQ_ERR_INVALID_ARG;
+    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (workspace_bytes < gq_pipelined_workspace_bytes(W, rank_stride, num_chunks)) return GQ_ERR_INVALID_ARG;
+    if (!aligned(d_out, 16) || !aligned(d_workspace, 256) || (d_codes_opt && !aligned(d_codes_opt, 16)) ||
+        (d_scales_opt && !aligned(d_scales_opt, 4)) || (d_found_inf_opt && !aligned(d_found_inf_opt, 4)))
+        return GQ_ERR_MISALIGNED;
+    const size_t gbytes = static_cast<size_t>(W) * rank_stride * elem_bytes_of(dt);
+    const size_t obytes = rank_stride * 4, cbytes = d_codes_opt ? static_cast<size_t>(W) * rank_stride : 0,
+                 sbytes = d_scales_opt ? static_cast<size_t>(W) * num_chunks * 4 : 0,
+                 fbytes = d_found_inf_opt ? 4 : 0;
+    const void* bufs[6] = {d_grads, d_out, d_codes_opt, d_scales_opt, d_found_inf_opt, d_workspace};
+    const size_t sizes[6] = {gbytes, obytes, cbytes, sbytes, fbytes, workspace_bytes};
+    for (int x = 0; x < 6; ++x)
+        for (int y = x + 1; y < 6; ++y)
+            if (overlaps(bufs[x], sizes[x], bufs[y], sizes[y])) return GQ_ERR_INVALID_ARG;
+    gq::QuantArgs a = quant_args(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
+    a.found_inf = d_found_inf_opt;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(dt == GQ_F32 ? gq::launch_pipe_f32(a, static_cast<int>(order), d_out, d_codes_opt, d_scales_opt,
+                                                        d_workspace, s)
+                                  : gq::launch_pipe_f16(a, static_cast<int>(order), d_out, d_codes_opt, d_scales_opt,
+                                                        d_workspace, s));
+}
+
 }  // extern "C"
 
 // ----------------------------------------------------------------- gq_fused_allreduce_sim_static

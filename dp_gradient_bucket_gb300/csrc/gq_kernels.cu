@@ -349,7 +349,9 @@ cudaError_t set_copy_stall(uint32_t extra_bytes, uint64_t limit_ns) {
     if ((e = fused_f32_set_stall(extra_bytes, limit_ns)) != cudaSuccess) return e;
     if ((e = fused_f16_set_stall(extra_bytes, limit_ns)) != cudaSuccess) return e;
     if ((e = queue_f32_set_stall(extra_bytes, limit_ns)) != cudaSuccess) return e;
-    return queue_f16_set_stall(extra_bytes, limit_ns);
+    if ((e = queue_f16_set_stall(extra_bytes, limit_ns)) != cudaSuccess) return e;
+    if ((e = pipe_f32_set_stall(extra_bytes, limit_ns)) != cudaSuccess) return e;
+    return pipe_f16_set_stall(extra_bytes, limit_ns);
 }
 
 cudaError_t read_and_clear_error_word(unsigned* word, cudaStream_t stream) {
@@ -365,6 +367,8 @@ cudaError_t read_and_clear_error_word(unsigned* word, cudaStream_t stream) {
     if ((e = fused_f16_read_clear_error(&w)) != cudaSuccess) return e;
     if ((e = queue_f32_read_clear_error(&w)) != cudaSuccess) return e;
     if ((e = queue_f16_read_clear_error(&w)) != cudaSuccess) return e;
+    if ((e = pipe_f32_read_clear_error(&w)) != cudaSuccess) return e;
+    if ((e = pipe_f16_read_clear_error(&w)) != cudaSuccess) return e;
     *word = w;
     return cudaSuccess;
 }

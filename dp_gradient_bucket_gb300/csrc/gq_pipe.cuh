@@ -1,0 +1,996 @@
+// gq_pipe.cuh -- the fused quantise + W-way reduce as a two-stage pipeline through L2.
+//
+// Same arithmetic as gq_fused.cuh ("pipelined HCCL AllReduce" article, bjdmk.com.cn/news/6235379,
+// §2.1 chunks, §2.2.1 quantize_gradient + INT8_ALLREDUCE, §3.1 one SUM per chunk, §6.1 unscale;
+// mean as in the "torchtitan-npu 3D parallel" article, AMP + 3D section), scheduled as the article's
+// §2.1 pipeline of quantise and allreduce stages, one persistent CTA per SM running both:
+//
+//   - Quantise items are (rank r, chunk j): one CTA owns the whole rank-chunk, as quantize_gradient
+//     sees it.  A producer lane bulk-copies it (cp.async.bulk, 16 KiB pieces, L2 evict_first) into a
+//     ring of shared-memory slots; quantiser warps take the absmax from shared memory (pass A), the
+//     scale, then quantise from shared memory again (pass B) and store the int8 codes to a workspace
+//     that stays in L2.  Each piece's slot is handed back to the producer as soon as pass B is done
+//     with it, so the copies of the next items are in flight while this one is quantised.  A chunk
+//     larger than the ring is copied twice (absmax pass, then quantise pass, the second from L2).
+//     The item then publishes one 64-bit word: this launch's tag and the scale bits, in one store.
+//   - Reduce items are (chunk j, segment t), t indexing torch.chunk(chunk, W) (the ring segments).
+//     Reducer warps wait (bounded) until the chunk's W words carry this launch's tag, read the
+//     segment's codes of every rank from L2 in the item's order, dequantise, sum, store the mean,
+//     and discard the code lines they alone read from L2 (discard.global.L2), so codes never travel
+//     to HBM.
+//   - Both kinds of item are claimed in chunk order from two 64-bit counters in the workspace, so
+//     every item is taken by a CTA that is running, quantise items never wait on reduce items, and
+//     every wait ends whatever the number of resident CTAs.
+//
+// HBM sees the algorithmic traffic only: gradients read once, the mean written once.
+#pragma once
+
+#include "gq_fused.cuh"
+
+namespace gq {
+namespace pipe {
+
+using fused::chunk_bounds;
+using fused::exact_u;
+using fused::fast_u;
+using fused::group_absmax;
+using fused::mean_of;
+using fused::raise_error;
+using fused::store_codes;
+
+constexpr int kPiece = 16384;  // bytes per bulk copy and per ring slot
+#ifndef GQ_PIPE_SLOTS
+#define GQ_PIPE_SLOTS 11
+#endif
+constexpr int kSlots = GQ_PIPE_SLOTS;  // 176 KiB of ring: a 128 KiB rank-chunk plus 48 KiB in flight
+#ifndef GQ_PIPE_QWARPS
+#define GQ_PIPE_QWARPS 16
+#endif
+#ifndef GQ_PIPE_RWARPS
+#define GQ_PIPE_RWARPS 4
+#endif
+constexpr int kQWarps = GQ_PIPE_QWARPS;  // quantiser warps
+constexpr int kRWarps = GQ_PIPE_RWARPS;  // reducer warps
+constexpr int kQThreads = 32 * kQWarps;
+constexpr int kRThreads = 32 * kRWarps;
+// warp 0 copies gradients into the ring, warp 1 copies codes into the reduce buffers
+constexpr int kThreads = 64 + kQThreads + kRThreads;
+constexpr int kInfo = 16;  // item descriptors in flight (> kSlots)
+constexpr int kGroupsPerPiece = kPiece / 16;
+constexpr int kQBar = 1;   // named barrier of the quantisers (0 is __syncthreads)
+// Reduce buffers: two, each holding one reduce unit's codes of every rank, a row per rank.  A unit
+// is at most r_unit(W) elements of one ring segment; its row holds the 16-byte-aligned bytes that
+// cover it (at most r_unit(W) + 32).
+#ifndef GQ_PIPE_RBUF_CODES
+#define GQ_PIPE_RBUF_CODES 16384
+#endif
+constexpr int kRBufCodes = GQ_PIPE_RBUF_CODES;
+constexpr int kRSlack = 32;
+constexpr int kRBufBytes = kRBufCodes + kMaxRanks * kRSlack;
+constexpr size_t kSmemBytes = static_cast<size_t>(kSlots) * kPiece + 2 * kRBufBytes;
+static_assert(kInfo > kSlots, "an item descriptor must outlive the pieces issued after it");
+// Each piece is worked on by a pair of quantiser warps, each taking half of its groups; piece p of an
+// item goes to pair p % kPairs, so a warp waits for, and hands back, only its own pieces.
+constexpr int kWarpsPerPiece = 2;
+constexpr int kPairs = kQWarps / kWarpsPerPiece;
+constexpr int kHalfGroups = kGroupsPerPiece / kWarpsPerPiece;  // groups per warp per piece
+constexpr int kGroupsPerLane = kHalfGroups / 32;
+static_assert(kQWarps % kWarpsPerPiece == 0 && kHalfGroups % 32 == 0, "piece split");
+// Items of at least this many pieces are copied twice (absmax pass, then quantise pass, the second
+// from L2) instead of being held in the ring whole; above kSlots pieces they must be.
+#ifndef GQ_PIPE_TWOPASS_PIECES
+#define GQ_PIPE_TWOPASS_PIECES (GQ_PIPE_SLOTS + 1)
+#endif
+constexpr int kTwoPassPieces = GQ_PIPE_TWOPASS_PIECES;
+static_assert(kTwoPassPieces >= 1 && kTwoPassPieces <= kSlots + 1, "two-pass threshold");
+static_assert(kThreads <= 1024, "block size");
+
+// Elements per reduce unit for W ranks: a multiple of 128 (so units of an aligned segment start on
+// L2 lines) with W rows of codes in kRBufCodes bytes.
+__host__ __device__ __forceinline__ int r_unit(int W) { return (kRBufCodes / W) / 128 * 128; }
+__host__ __device__ __forceinline__ int r_row(int W) { return r_unit(W) + kRSlack; }
+
+// Workspace: a 256-byte header, one 64-bit word per (chunk, rank) at j * W + r, then the codes,
+// W rows of cstride bytes (cstride = rank_stride rounded up to 128, so rows start on L2 lines).
+struct Hdr {
+    unsigned long long q_head;  // next quantise item
+    unsigned long long r_head;  // next reduce item
+    unsigned exit_count;        // CTAs of this launch that have left
+    unsigned epoch;             // launches completed (mod 2^32 - 1): the tag is epoch + 1
+};
+constexpr size_t kHdrBytes = 256;
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline size_t tag_region_bytes(int64_t num_chunks, int W) {
+    return align_up(static_cast<size_t>(num_chunks) * static_cast<size_t>(W) * 8, 256);
+}
+inline int64_t code_stride(int64_t rank_stride) { return static_cast<int64_t>(align_up(rank_stride, 128)); }
+inline size_t workspace_bytes(int W, int64_t rank_stride, int64_t num_chunks) {
+    return kHdrBytes + tag_region_bytes(num_chunks, W) + static_cast<size_t>(W) * code_stride(rank_stride);
+}
+
+struct PArgs {
+    QuantArgs q;
+    int order;
+    float* out;
+    int8_t* codes_out;  // [W][rank_stride], may be null
+    float* scales_out;  // [W][num_chunks], may be null
+    float invW;
+    int w_pow2;
+    // -0.0f, as a kernel argument: fma(a, b, neg_zero) rounds a * b exactly once, like a multiply,
+    // and, its addend being unknown to the compiler, can be neither turned back into a multiply
+    // nor fused with the addition that follows (packed multiplies and adds are contracted otherwise)
+    float neg_zero;
+    Hdr* hdr;
+    uint64_t* tags;   // [num_chunks][W]
+    int8_t* wcodes;   // [W][cstride]
+    int64_t cstride;
+    unsigned long long total_q, total_r;
+    size_t tag_words;
+};
+
+// One quantise item as the producer hands it to the quantisers.
+struct Info {
+    int64_t lo, hi;  // the chunk's elements
+    int64_t g0;      // first 16-byte group copied (the row's 16-byte grid)
+    int64_t j;       // chunk
+    int64_t bytes;   // bytes copied: whole groups covering [lo, hi)
+    int r;           // rank
+    int np;          // pieces per pass
+    int twopass;     // the chunk is larger than the ring: copied once per pass
+    int valid;       // 0: no more items
+};
+
+// One reduce unit as its producer hands it to the reducers.
+struct RInfo {
+    int64_t a, b;  // elements of one ring segment
+    int64_t c0;    // first code byte copied (16-byte aligned)
+    int rot;       // first rank of the summation order
+    int valid;     // 0: no more units
+    float s[kMaxRanks];  // the chunk's scales, by rank
+};
+
+struct Shared {
+    uint64_t full[kSlots];   // a piece has landed in the slot (producer arrival + bytes)
+    uint64_t empty[kSlots];  // both quantiser warps of the piece are done with the slot
+    uint64_t rfull[2];       // a reduce unit's codes have landed
+    uint64_t rempty[2];      // every reducer warp is done with the buffer
+    Info info[kInfo];
+    RInfo rinfo[2];
+    uint32_t issued[kSlots];  // phases started on full[] (to let copies land before exit)
+    uint32_t rissued[2];
+    uint32_t qmax[2][kQWarps];
+    uint32_t tag;
+    int abort;
+    int last;
+};
+
+// ----------------------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ void named_bar(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Named barrier that also returns whether `pred` held in any participating thread.
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy accesses (the acquire of a scale word) before its later
+// async-proxy accesses (the bulk copies of the codes that word published).
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t ld_shared_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)));
+    return v;
+}
+
+// Packed pairs of binary32 (f32x2): each half rounds exactly as the scalar operation would.
+__device__ __forceinline__ uint64_t pk(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpk(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// (the compiler contracts a packed multiply into a packed add that uses its result, .rn or not:
+// use fma2 with a runtime -0 addend for a product that is added afterwards)
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// a * b + c with one rounding (used only in the near-tie filter, never for a result)
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// max(m, |a|, |b|), NaN propagated (a NaN orders above every number in the final bit pattern).
+__device__ __forceinline__ float absmax3(float m, float a, float b) {
+    float r;
+    asm("{\n\t.reg .f32 ta, tb;\n\tabs.f32 ta, %2;\n\tabs.f32 tb, %3;\n\tmax.NaN.f32 %0, %1, ta, tb;\n\t}"
+        : "=f"(r)
+        : "f"(m), "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void st_hint_u32(void* p, uint32_t v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(policy) : "memory");
+}
+
+__device__ __forceinline__ void st_hint_u64(void* p, uint64_t v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.b64 [%0], %1, %2;" ::"l"(p), "l"(v), "l"(policy) : "memory");
+}
+
+// Drop a 128-byte L2 line without writing it back (its codes have been read for the last time).
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+__device__ __forceinline__ int ld_volatile_int(const int* p) { return *static_cast<const volatile int*>(p); }
+__device__ __forceinline__ void st_volatile_int(int* p, int v) { *static_cast<volatile int*>(p) = v; }
+
+// Wait for phase `parity` of a slot barrier; false after `limit_ns`, or as soon as the CTA aborts.
+#ifndef GQ_PIPE_WAIT_SLEEP_NS
+#define GQ_PIPE_WAIT_SLEEP_NS 0
+#endif
+__device__ __forceinline__ bool wait_slot(uint64_t* bar, uint32_t parity, uint64_t limit_ns, const int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (GQ_PIPE_WAIT_SLEEP_NS > 0) __nanosleep(GQ_PIPE_WAIT_SLEEP_NS);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (ld_volatile_int(abort) || global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// wait_slot for a whole warp: every lane gets the same answer (false if any lane gave up), so the
+// warp's control flow stays uniform.
+__device__ __forceinline__ bool warp_wait_slot(uint64_t* bar, uint32_t parity, uint64_t limit_ns, const int* abort) {
+    const bool ok = wait_slot(bar, parity, limit_ns, abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// ----------------------------------------------------------------------------- producer
+
+template <int DT>
+__device__ void producer(const PArgs& P, Shared& S, unsigned char* ring, uint32_t tag, uint64_t limit) {
+    constexpr int VEC = DT == 0 ? 4 : 8;
+    constexpr int EB = DT == 0 ? 4 : 2;
+    const unsigned long long W = static_cast<unsigned long long>(P.q.W);
+    const int64_t n = P.q.num_chunks;
+    const char* grads = static_cast<const char*>(P.q.grads);
+    const int64_t row_bytes = P.q.rank_stride * EB;
+    const uint64_t once = l2_policy_evict_first(), again = l2_policy_evict_last();
+    uint32_t extra = fused::g_stall_extra_tx;  // fault injection: the first copy never completes
+    uint32_t seq = 0;  // pieces issued
+    uint32_t k = 0;    // items handed over
+    bool ok = true;
+    // slot of piece s is free once the quantisers released its previous use (piece s - kSlots)
+    auto acquire = [&](uint32_t s) -> bool {
+        if (s < static_cast<uint32_t>(kSlots)) return true;
+        if (wait_slot(&S.empty[s % kSlots], ((s / kSlots) - 1u) & 1u, limit, &S.abort)) return true;
+        if (!ld_volatile_int(&S.abort)) raise_error(kErrTimeout);
+        st_volatile_int(&S.abort, 1);
+        return false;
+    };
+    unsigned long long item = atomicAdd(&P.hdr->q_head, 1ull);
+    while (item < P.total_q && !ld_volatile_int(&S.abort)) {
+        const unsigned long long next = atomicAdd(&P.hdr->q_head, 1ull);  // used after this item
+        const int64_t j = static_cast<int64_t>(item / W);
+        const int r = static_cast<int>(item % W);
+        int64_t lo, hi;
+        if (!chunk_bounds(P.q.offsets, j, n, P.q.rank_stride, &lo, &hi)) {
+            if (r == 0) raise_error(kErrBadTable);  // its reduce items skip it too
+            item = next;
+            continue;
+        }
+        if (hi == lo) {  // empty chunk: scale 0, no codes
+            if (P.scales_out) P.scales_out[static_cast<int64_t>(r) * n + j] = 0.0f;
+            st_relaxed_gpu_u64(P.tags + j * P.q.W + r, static_cast<uint64_t>(tag) << 32);
+            item = next;
+            continue;
+        }
+        const int64_t g0 = lo / VEC, g1 = (hi + VEC - 1) / VEC;
+        const int64_t bytes = (g1 - g0) * 16;
+        const int np = static_cast<int>((bytes + kPiece - 1) / kPiece);
+        const int twopass = np >= kTwoPassPieces ? 1 : 0;
+        Info& in = S.info[k % kInfo];
+        in.lo = lo;
+        in.hi = hi;
+        in.g0 = g0;
+        in.j = j;
+        in.bytes = bytes;
+        in.r = r;
+        in.np = np;
+        in.twopass = twopass;
+        in.valid = 1;
+        const char* src = grads + r * row_bytes + g0 * 16;
+        for (int pass = 0; pass <= twopass && ok; ++pass) {
+            for (int p = 0; p < np; ++p) {
+                if (!acquire(seq)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t slot = seq % kSlots;
+                const int64_t left = bytes - static_cast<int64_t>(p) * kPiece;
+                const uint32_t nb = static_cast<uint32_t>(left < kPiece ? left : kPiece);
+                mbar_arrive_expect_tx(&S.full[slot], nb + extra);
+                extra = 0;
+                bulk_copy_g2s_hint(ring + static_cast<size_t>(slot) * kPiece, src + static_cast<int64_t>(p) * kPiece, nb,
+                                   &S.full[slot], (twopass && pass == 0) ? again : once);
+                S.issued[slot] += 1u;
+                ++seq;
+            }
+        }
+        if (!ok) break;
+        ++k;
+        item = next;
+    }
+    // no more items: a descriptor marked invalid, signalled by a plain arrival on the next slot
+    if (ok && acquire(seq)) {
+        const uint32_t slot = seq % kSlots;
+        S.info[k % kInfo].valid = 0;
+        mbar_arrive(&S.full[slot]);
+        S.issued[slot] += 1u;
+    }
+}
+
+// ----------------------------------------------------------------------------- quantisers
+
+// Near-tie filter bound: rd((0.5 - 2^-14)^2).  An element is sent to the exact division when
+// fl(d * d - kTieSq) >= 0 (sign bit clear), d = t - rne(t): that holds for every |d| >= sqrt(kTieSq),
+// which includes every |d| > 0.5 - 2^-14 (the bound of fast_u), so the filter only ever adds
+// elements to the exact path.
+constexpr uint32_t kTieSqBits = 0x3E7FF000u;  // 0.2499389648... <= (0.5 - 2^-14)^2 = 0.2499389686...
+
+// Pass A over one 16-byte group: running absmax, as a float for whole fp32 groups (NaN kept) and
+// as |x| bit patterns otherwise.
+template <int DT>
+__device__ __forceinline__ void absmax_group(const V16& v, int64_t e0, bool full, int64_t lo, int64_t hi, float& mf,
+                                             uint32_t& mi) {
+    if (DT == 0 && full) {
+        mf = absmax3(mf, __uint_as_float(v.w[0]), __uint_as_float(v.w[1]));
+        mf = absmax3(mf, __uint_as_float(v.w[2]), __uint_as_float(v.w[3]));
+    } else {
+        mi = group_absmax<DT>(v, e0, full, lo, hi, mi);
+    }
+}
+
+// Pass B over one 16-byte group: the codes of its VEC elements, packed 4 per word.  Pairs of
+// elements go through the packed f32x2 form of fast_u: t = x * c, u = t + M, d = t - (u - M);
+// if any d lies near +-1/2 (the filter above) every element of the group is redone exactly.
+template <int DT>
+__device__ __forceinline__ void quantise_group(const V16& v, uint64_t c2, uint64_t z2, bool exact_all, float inv,
+                                               bool scaled, const ScaleQ& sq, uint32_t (&packed)[DT == 0 ? 1 : 2]) {
+    constexpr int VEC = DT == 0 ? 4 : 8;
+    const uint64_t M2 = pk(kMagic, kMagic);
+    const uint64_t NT2 = pk(-__uint_as_float(kTieSqBits), -__uint_as_float(kTieSqBits));
+    float u[VEC];
+    uint32_t all_far = 0xffffffffu;
+#pragma unroll
+    for (int e = 0; e < VEC; e += 2) {
+        const uint64_t x = pk(group_elem<DT>(v, e), group_elem<DT>(v, e + 1));
+        const uint64_t t = fma2(x, c2, z2);  // fl(x * c), never contracted into the addition below
+        const uint64_t uu = add2(t, M2);
+        const uint64_t d = sub2(t, sub2(uu, M2));
+        float z0, z1;
+        unpk(fma2(d, d, NT2), z0, z1);
+        all_far &= __float_as_uint(z0) & __float_as_uint(z1);
+        unpk(uu, u[e], u[e + 1]);
+    }
+    if (exact_all || !(all_far >> 31)) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) u[e] = exact_u(group_elem<DT>(v, e), inv, scaled, sq);
+    }
+#pragma unroll
+    for (int q = 0; q < VEC / 4; ++q) {
+        const uint32_t lo16 = __byte_perm(__float_as_uint(u[4 * q]), __float_as_uint(u[4 * q + 1]), 0x0040u);
+        const uint32_t hi16 = __byte_perm(__float_as_uint(u[4 * q + 2]), __float_as_uint(u[4 * q + 3]), 0x0040u);
+        packed[q] = __byte_perm(lo16, hi16, 0x5410u);
+    }
+}
+
+template <int DT>
+__device__ void quantiser(const PArgs& P, Shared& S, const unsigned char* ring, uint32_t tag, uint64_t limit,
+                          int qtid) {
+    constexpr int VEC = DT == 0 ? 4 : 8;
+    const int lane = qtid & 31, qwarp = qtid >> 5;
+    const int pair = qwarp / kWarpsPerPiece;
+    const uint32_t half = static_cast<uint32_t>(qwarp % kWarpsPerPiece);
+    const int W = P.q.W;
+    const int64_t n = P.q.num_chunks;
+    const float inv = P.q.inv;
+    const bool scaled = P.q.scaled != 0;
+    const uint64_t keep = l2_policy_evict_last();
+    uint32_t cseq = 0;       // pieces consumed
+    bool fail = false;       // a wait of this warp gave up
+    bool aborted = false;    // a wait of some quantiser gave up: every quantiser leaves
+    bool have_prev = false;  // an item is waiting to be published
+    int64_t prev_j = 0;
+    int prev_r = 0;
+    float prev_s = 0.0f;
+
+    for (uint32_t k = 0;; ++k) {
+        // ---- next item: its first piece has landed (or the end marker was posted)
+        const bool ok = !fail && warp_wait_slot(&S.full[cseq % kSlots], (cseq / kSlots) & 1u, limit, &S.abort);
+        Info in;
+        in.valid = 0;
+        if (ok) in = S.info[k % kInfo];
+        if (named_bar_or(kQBar, kQThreads, !ok)) {  // a wait gave up somewhere: abort
+            aborted = true;
+            break;
+        }
+        // every quantiser finished the previous item's code stores before this barrier: publish it
+        if (have_prev && qtid == 0) {
+            fence_acq_rel_gpu();
+            st_relaxed_gpu_u64(P.tags + prev_j * W + prev_r,
+                               (static_cast<uint64_t>(tag) << 32) | __float_as_uint(prev_s));
+        }
+        if (!in.valid) break;  // uniform: every thread read the same descriptor
+
+        // ---- pass A: absmax over the rank-chunk
+        // groups are numbered from the item's first (32-bit); groups [gf0, gf0 + gfull) lie wholly
+        // inside the chunk, only the first and the last can stick out of it
+        const uint32_t ngroups = static_cast<uint32_t>(in.bytes / 16);
+        const uint32_t gf0 = (in.lo % VEC) != 0 ? 1u : 0u;
+        const uint32_t gend = ngroups - ((in.hi % VEC) != 0 ? 1u : 0u);
+        const uint32_t gfull = gend > gf0 ? gend - gf0 : 0u;
+        float mf = 0.0f;
+        uint32_t mi = 0;
+        for (int p = pair; p < in.np && !fail; p += kPairs) {
+            const uint32_t s = cseq + static_cast<uint32_t>(p);
+            const uint32_t slot = s % kSlots;
+            if (p > 0 && !warp_wait_slot(&S.full[slot], (s / kSlots) & 1u, limit, &S.abort)) {
+                fail = true;
+                break;
+            }
+            const uint32_t gp = static_cast<uint32_t>(p) * kGroupsPerPiece + half * kHalfGroups;  // this warp's first
+            const uint32_t ng = gp < ngroups ? min(static_cast<uint32_t>(kHalfGroups), ngroups - gp) : 0u;
+            const unsigned char* base = ring + static_cast<size_t>(slot) * kPiece + half * (kHalfGroups * 16);
+            if (DT == 0 && ng == kHalfGroups && gp - gf0 < gfull && gp + ng <= gf0 + gfull) {
+                // a full half-piece of whole groups: a fixed share per lane, no tests
+#pragma unroll 8
+                for (int k = 0; k < kGroupsPerLane; ++k) {
+                    const V16 v = ld_shared_v16(base + (lane + 32 * k) * 16);
+                    mf = absmax3(mf, __uint_as_float(v.w[0]), __uint_as_float(v.w[1]));
+                    mf = absmax3(mf, __uint_as_float(v.w[2]), __uint_as_float(v.w[3]));
+                }
+            } else {
+#pragma unroll 1
+                for (uint32_t gl = lane; gl < ng; gl += 32) {
+                    const V16 v = ld_shared_v16(base + gl * 16);
+                    const uint32_t gi = gp + gl;
+                    if (gi - gf0 < gfull) {  // a whole group inside the chunk
+                        if (DT == 0) {
+                            mf = absmax3(mf, __uint_as_float(v.w[0]), __uint_as_float(v.w[1]));
+                            mf = absmax3(mf, __uint_as_float(v.w[2]), __uint_as_float(v.w[3]));
+                        } else {
+                            mi = group_absmax<DT>(v, 0, true, 0, 0, mi);
+                        }
+                    } else {
+                        mi = group_absmax<DT>(v, (in.g0 + gi) * VEC, false, in.lo, in.hi, mi);
+                    }
+                }
+            }
+            if (in.twopass) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&S.empty[slot]);
+            }
+        }
+        uint32_t m = max(__float_as_uint(mf) & 0x7fffffffu, mi);
+        m = __reduce_max_sync(0xffffffffu, m);
+        if (lane == 0) S.qmax[k & 1u][qwarp] = m;
+        if (named_bar_or(kQBar, kQThreads, fail)) {
+            aborted = true;
+            break;
+        }
+        uint32_t mraw = 0;
+#pragma unroll
+        for (int w = 0; w < kQWarps; ++w) mraw = max(mraw, S.qmax[k & 1u][w]);
+        float mx = DT == 0 ? __uint_as_float(mraw) : __half2float(__ushort_as_half(static_cast<unsigned short>(mraw)));
+        if (scaled) mx = __fmul_rn(mx, inv);  // max|fl(x*inv)| = fl(max|x| * inv): rounding is monotone
+        const ScaleQ sq = make_scale(mx);
+        if (qtid == 0) {
+            const bool nonfinite = (DT == 0 ? mraw >= 0x7f800000u : mraw >= 0x7c00u) || !(fabsf(mx) <= 3.40282347e38f);
+            if (nonfinite) {
+                raise_error(kErrNonfinite);
+                if (P.q.found_inf) *P.q.found_inf = 1.0f;
+            }
+            if (P.scales_out) P.scales_out[static_cast<int64_t>(in.r) * n + in.j] = sq.s;
+        }
+        // zero scale: c = 0 gives t = 0 and code 0 on the fast path; subnormal scale: exact always
+        const float c = sq.mode == 1 ? (scaled ? __fmul_rn(inv, sq.rcp) : sq.rcp) : 0.0f;
+        const uint64_t c2 = pk(c, c);
+        const uint64_t z2 = pk(P.neg_zero, P.neg_zero);
+        const bool exact_all = sq.mode == 2;
+
+        // ---- pass B: quantise from shared memory, codes to the workspace (and the caller's buffer)
+        const uint32_t bseq = in.twopass ? cseq + static_cast<uint32_t>(in.np) : cseq;
+        int8_t* crow = P.wcodes + static_cast<int64_t>(in.r) * P.cstride;
+        int8_t* urow = P.codes_out ? P.codes_out + static_cast<int64_t>(in.r) * P.q.rank_stride : nullptr;
+        int8_t* cbase = crow + in.g0 * VEC;  // code of the item's first group
+        int8_t* ubase = urow ? urow + in.g0 * VEC : nullptr;
+        for (int p = pair; p < in.np && !fail; p += kPairs) {
+            const uint32_t s = bseq + static_cast<uint32_t>(p);
+            const uint32_t slot = s % kSlots;
+            if (in.twopass && !warp_wait_slot(&S.full[slot], (s / kSlots) & 1u, limit, &S.abort)) {
+                fail = true;
+                break;
+            }
+            const uint32_t gp = static_cast<uint32_t>(p) * kGroupsPerPiece + half * kHalfGroups;
+            const uint32_t ng = gp < ngroups ? min(static_cast<uint32_t>(kHalfGroups), ngroups - gp) : 0u;
+            const unsigned char* base = ring + static_cast<size_t>(slot) * kPiece + half * (kHalfGroups * 16);
+            if (ng == kHalfGroups && gp - gf0 < gfull && gp + ng <= gf0 + gfull && !urow) {
+                // a full half-piece of whole groups, codes to the workspace only
+#pragma unroll 4
+                for (int k = 0; k < kGroupsPerLane; ++k) {
+                    const uint32_t gl = lane + 32 * k;
+                    const V16 v = ld_shared_v16(base + gl * 16);
+                    uint32_t packed[VEC / 4];
+                    quantise_group<DT>(v, c2, z2, exact_all, inv, scaled, sq, packed);
+                    if (VEC == 4)
+                        st_hint_u32(cbase + (gp + gl) * VEC, packed[0], keep);
+                    else
+                        st_hint_u64(cbase + (gp + gl) * VEC,
+                                    (static_cast<uint64_t>(packed[VEC / 4 - 1]) << 32) | packed[0], keep);
+                }
+            } else {
+#pragma unroll 1
+                for (uint32_t gl = lane; gl < ng; gl += 32) {
+                    const V16 v = ld_shared_v16(base + gl * 16);
+                    const uint32_t gi = gp + gl;
+                    uint32_t packed[VEC / 4];
+                    quantise_group<DT>(v, c2, z2, exact_all, inv, scaled, sq, packed);
+                    if (gi - gf0 < gfull) {
+                        if (VEC == 4)
+                            st_hint_u32(cbase + gi * VEC, packed[0], keep);
+                        else
+                            st_hint_u64(cbase + gi * VEC,
+                                        (static_cast<uint64_t>(packed[VEC / 4 - 1]) << 32) | packed[0], keep);
+                        if (urow) store_codes<VEC>(ubase + gi * VEC, 0, true, 0, 0, packed);
+                    } else {
+                        const int64_t e0 = (in.g0 + gi) * VEC;
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            if (e0 + e >= in.lo && e0 + e < in.hi)
+                                crow[e0 + e] = static_cast<int8_t>((packed[e >> 2] >> (8 * (e & 3))) & 0xffu);
+                        if (urow) store_codes<VEC>(urow, e0, false, in.lo, in.hi, packed);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&S.empty[slot]);
+        }
+        cseq = bseq + static_cast<uint32_t>(in.np);
+        have_prev = !fail;
+        prev_j = in.j;
+        prev_r = in.r;
+        prev_s = sq.s;
+    }
+    if (qtid == 0 && aborted) {
+        if (!ld_volatile_int(&S.abort)) raise_error(kErrTimeout);
+        st_volatile_int(&S.abort, 1);
+    }
+}
+
+// ----------------------------------------------------------------------------- reduce producer
+
+// One warp: claims reduce items (chunk j, ring segment t) in order, waits (bounded) until the
+// chunk's W scale words carry this launch's tag -- lane r reads rank r's word, all in parallel --
+// then bulk-copies the segment's codes of every rank (lane r issues rank r's copy), one unit of at
+// most r_unit(W) elements at a time, into the two reduce buffers in turn.  Control flow is uniform
+// across the warp; lane 0 alone claims items and arrives on barriers.
+static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf, uint32_t tag, uint64_t limit) {
+    const int lane = threadIdx.x & 31;
+    const int W = P.q.W;
+    const unsigned long long UW = static_cast<unsigned long long>(W);
+    const int64_t n = P.q.num_chunks;
+    const bool ring = P.order == fused::kOrderRing;
+    const int64_t E = r_unit(W);
+    const uint32_t row = static_cast<uint32_t>(r_row(W));
+    const uint64_t once = l2_policy_evict_first();
+    uint32_t useq = 0;  // units handed over
+    bool ok = true;
+    auto fail_now = [&]() {
+        if (lane == 0) {
+            if (!ld_volatile_int(&S.abort)) raise_error(kErrTimeout);
+            st_volatile_int(&S.abort, 1);
+        }
+    };
+    auto acquire = [&](uint32_t u) -> bool {  // buffer of unit u is free (its unit u - 2 released)
+        if (u < 2u) return true;
+        return warp_wait_slot(&S.rempty[u & 1u], ((u >> 1) - 1u) & 1u, limit, &S.abort);
+    };
+    unsigned long long item = 0, next = 0;
+    if (lane == 0) {
+        item = atomicAdd(&P.hdr->r_head, 1ull);
+        next = atomicAdd(&P.hdr->r_head, 1ull);
+    }
+    item = __shfl_sync(0xffffffffu, item, 0);
+    for (;;) {
+        if (item >= P.total_r || ld_volatile_int(&S.abort)) break;
+        const int64_t j = static_cast<int64_t>(item / UW);
+        const int t = static_cast<int>(item % UW);
+        // claim the item after next now: its latency hides behind this one
+        unsigned long long after = 0;
+        if (lane == 0) after = atomicAdd(&P.hdr->r_head, 1ull);
+        item = __shfl_sync(0xffffffffu, next, 0);
+        next = after;
+        int64_t lo, hi;
+        if (!chunk_bounds(P.q.offsets, j, n, P.q.rank_stride, &lo, &hi) || hi == lo) continue;
+        const int64_t seg = (hi - lo + W - 1) / W;  // torch.chunk(chunk, W) piece length
+        const int64_t a = min(hi, lo + static_cast<int64_t>(t) * seg), b = min(hi, a + seg);
+        if (b <= a) continue;
+        // the chunk's W words must carry this launch's tag (each is published after its codes)
+        const uint64_t* words = P.tags + j * W;
+        float s_lo = 0.0f, s_hi = 0.0f;  // scales of ranks lane and lane + 32
+        uint64_t t0 = 0;
+        for (int tries = 0;; ++tries) {
+            bool mine = true;
+            if (lane < W) {
+                const uint64_t w = ld_relaxed_gpu_u64(words + lane);
+                mine = static_cast<uint32_t>(w >> 32) == tag;
+                s_lo = __uint_as_float(static_cast<uint32_t>(w));
+            }
+            if (lane + 32 < W) {
+                const uint64_t w = ld_relaxed_gpu_u64(words + lane + 32);
+                mine = mine && static_cast<uint32_t>(w >> 32) == tag;
+                s_hi = __uint_as_float(static_cast<uint32_t>(w));
+            }
+            if (__all_sync(0xffffffffu, mine)) break;
+            if (tries == 0) t0 = global_timer_ns();
+            const int late = ld_volatile_int(&S.abort) || global_timer_ns() - t0 > limit;
+            if (__shfl_sync(0xffffffffu, late, 0)) {
+                ok = false;
+                break;
+            }
+            __nanosleep(64);
+        }
+        if (!ok) {
+            fail_now();
+            break;
+        }
+        fence_acq_rel_gpu();         // acquire: the codes stored before the words
+        fence_proxy_async_global();  // ... and before the bulk copies that read them
+        const int rot = ring ? (t + 1 == W ? 0 : t + 1) : 0;
+        for (int64_t x = a; x < b; x += E) {
+            if (!acquire(useq)) {
+                ok = false;
+                break;
+            }
+            const uint32_t buf = useq & 1u;
+            const int64_t xb = min(b, x + E);
+            const int64_t c0 = x & ~static_cast<int64_t>(15);
+            const uint32_t nb = static_cast<uint32_t>(((xb + 15) & ~static_cast<int64_t>(15)) - c0);
+            RInfo& ri = S.rinfo[buf];
+            if (lane == 0) {
+                ri.a = x;
+                ri.b = xb;
+                ri.c0 = c0;
+                ri.rot = rot;
+                ri.valid = 1;
+            }
+            if (lane < W) ri.s[lane] = s_lo;
+            if (lane + 32 < W) ri.s[lane + 32] = s_hi;
+            __syncwarp();  // the descriptor is written before lane 0's arrival publishes it
+            if (lane == 0) mbar_arrive_expect_tx(&S.rfull[buf], nb * static_cast<uint32_t>(W));
+            __syncwarp();  // the expected bytes are posted before any copy can complete them
+            unsigned char* dst = rbuf + buf * kRBufBytes;
+            for (int r = lane; r < W; r += 32)
+                bulk_copy_g2s_hint(dst + r * row, P.wcodes + static_cast<int64_t>(r) * P.cstride + c0, nb, &S.rfull[buf],
+                                   once);
+            if (lane == 0) S.rissued[buf] += 1u;
+            ++useq;
+        }
+        if (!ok) {
+            fail_now();
+            break;
+        }
+    }
+    // no more units: a descriptor marked invalid, signalled by a plain arrival on the next buffer
+    if (ok && !ld_volatile_int(&S.abort) && acquire(useq)) {
+        const uint32_t buf = useq & 1u;
+        if (lane == 0) {
+            S.rinfo[buf].valid = 0;
+            mbar_arrive(&S.rfull[buf]);
+            S.rissued[buf] += 1u;
+        }
+    } else if (ok) {
+        fail_now();
+    }
+}
+
+// ----------------------------------------------------------------------------- reducers
+
+// int8 code e (0..3) of a word whose bytes were XOR-ed with 0x80 (so byte = q + 128), as the
+// float 2^23 + 128 + q: the byte becomes the low mantissa byte of 2^23.
+__device__ __forceinline__ float code_biased(uint32_t wx, int e) {
+    return __uint_as_float(__byte_perm(wx, 0x4B000000u, 0x7540u | static_cast<uint32_t>(e)));
+}
+constexpr float kCodeBias = 8388736.0f;  // 2^23 + 128: code_biased - kCodeBias = q exactly
+
+// Elements [e0, e0 + 16) of a reduce unit under the sequential or ring order, from the unit's rows
+// in shared memory (row r at base + r * row, element e at byte e - c0): per rank in the order
+// from `rot`, 16 codes dequantised (q * s, one rounding) and added, a pair of elements per packed
+// f32x2 operation; the mean of the elements in [a, b) is stored.
+__device__ __forceinline__ void reduce_group16(const PArgs& P, const unsigned char* base, uint32_t row, const float* sc,
+                                               int W, int rot, int64_t e0, int64_t c0, int64_t a, int64_t b, bool pow2) {
+    const uint64_t C2 = pk(kCodeBias, kCodeBias);
+    const uint64_t z2 = pk(P.neg_zero, P.neg_zero);
+    const uint32_t off = static_cast<uint32_t>(e0 - c0);
+    uint64_t acc[8];
+    for (int k = 0; k < W; ++k) {
+        int r = rot + k;
+        r -= r >= W ? W : 0;
+        const V16 w = ld_shared_v16(base + r * row + off);
+        const float s = sc[r];
+        const uint64_t s2 = pk(s, s);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t wx = w.w[q] ^ 0x80808080u;
+            // q * s rounded once (fma with a -0 addend), then one rounded addition
+            const uint64_t p0 = fma2(sub2(pk(code_biased(wx, 0), code_biased(wx, 1)), C2), s2, z2);
+            const uint64_t p1 = fma2(sub2(pk(code_biased(wx, 2), code_biased(wx, 3)), C2), s2, z2);
+            acc[2 * q] = k == 0 ? p0 : add2(acc[2 * q], p0);
+            acc[2 * q + 1] = k == 0 ? p1 : add2(acc[2 * q + 1], p1);
+        }
+    }
+    float o[16];
+    if (pow2) {
+        const uint64_t iw = pk(P.invW, P.invW);  // acc * (1/W) rounds the same exact value as acc / W
+#pragma unroll
+        for (int q = 0; q < 8; ++q) unpk(mul2(acc[q], iw), o[2 * q], o[2 * q + 1]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float x0, x1;
+            unpk(acc[q], x0, x1);
+            o[2 * q] = __fdiv_rn(x0, static_cast<float>(W));
+            o[2 * q + 1] = __fdiv_rn(x1, static_cast<float>(W));
+        }
+    }
+    if (e0 >= a && e0 + 16 <= b) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4*>(P.out + e0 + 4 * q) = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            if (e0 + e >= a && e0 + e < b) P.out[e0 + e] = o[e];
+    }
+}
+
+// The same under the tree order, two elements at a time (ranks in index order).
+__device__ __forceinline__ void reduce_group16_tree(const PArgs& P, const unsigned char* base, uint32_t row,
+                                                   const float* sc, int W, int64_t e0, int64_t c0, int64_t a,
+                                                   int64_t b, bool pow2) {
+#pragma unroll 1
+    for (int q = 0; q < 8; ++q) {
+        const int64_t f0 = e0 + 2 * q;
+        if (f0 + 2 <= a || f0 >= b) continue;
+        const uint32_t off = static_cast<uint32_t>(f0 - c0);
+        TreeAcc tr[2];
+        tr[0].init();
+        tr[1].init();
+        for (int r = 0; r < W; ++r) {
+            const uint32_t wx = (ld_shared_u32(base + r * row + (off & ~3u)) >> (8 * (off & 3u))) ^ 0x8080u;
+            const float s = sc[r];
+            tr[0].push(__fmul_rn(__fsub_rn(code_biased(wx, 0), kCodeBias), s));
+            tr[1].push(__fmul_rn(__fsub_rn(code_biased(wx, 1), kCodeBias), s));
+        }
+        const float o0 = mean_of(tr[0].result(), W, P.invW, pow2), o1 = mean_of(tr[1].result(), W, P.invW, pow2);
+        if (f0 >= a && f0 + 2 <= b) {
+            *reinterpret_cast<float2*>(P.out + f0) = make_float2(o0, o1);
+        } else {
+            if (f0 >= a && f0 < b) P.out[f0] = o0;
+            if (f0 + 1 >= a && f0 + 1 < b) P.out[f0 + 1] = o1;
+        }
+    }
+}
+
+static __device__ void reducer(const PArgs& P, Shared& S, const unsigned char* rbuf, uint64_t limit, int rtid) {
+    const int lane = rtid & 31;
+    const int W = P.q.W;
+    const uint32_t row = static_cast<uint32_t>(r_row(W));
+    const bool pow2 = P.w_pow2 != 0;
+    const bool tree = P.order == fused::kOrderTree;
+    for (uint32_t useq = 0;; ++useq) {
+        const uint32_t buf = useq & 1u;
+        if (!warp_wait_slot(&S.rfull[buf], (useq >> 1) & 1u, limit, &S.abort)) {
+            if (lane == 0) {
+                if (!ld_volatile_int(&S.abort)) raise_error(kErrTimeout);
+                st_volatile_int(&S.abort, 1);
+            }
+            break;
+        }
+        const RInfo& ri = S.rinfo[buf];
+        if (!ri.valid) break;
+        const int64_t a = ri.a, b = ri.b, c0 = ri.c0;
+        const int rot = ri.rot;
+        const unsigned char* base = rbuf + buf * kRBufBytes;
+        const int64_t G0 = a / 16, G1 = (b + 15) / 16;
+        for (int64_t G = G0 + rtid; G < G1; G += kRThreads) {
+            if (tree)
+                reduce_group16_tree(P, base, row, ri.s, W, G * 16, c0, a, b, pow2);
+            else
+                reduce_group16(P, base, row, ri.s, W, rot, G * 16, c0, a, b, pow2);
+        }
+        // the code lines of every rank wholly inside [a, b) were read for the last time by this
+        // unit's copies: drop them from L2 without a write-back
+        const int64_t l0 = (a + 127) / 128, l1 = b / 128;
+        const int nl = l1 > l0 ? static_cast<int>(l1 - l0) : 0;
+        for (int x = rtid; x < nl * W; x += kRThreads)
+            discard_l2_line(P.wcodes + static_cast<int64_t>(x / nl) * P.cstride + (l0 + x % nl) * 128);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.rempty[buf]);
+    }
+}
+
+// ----------------------------------------------------------------------------- kernel
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) k_pipe(const PArgs P) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ Shared S;
+    unsigned char* ring = smem;
+    unsigned char* rbuf = smem + static_cast<size_t>(kSlots) * kPiece;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&S.full[s], 1);
+            mbar_init(&S.empty[s], kWarpsPerPiece);
+            S.issued[s] = 0;
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&S.rfull[b], 1);
+            mbar_init(&S.rempty[b], kRWarps);
+            S.rissued[b] = 0;
+        }
+        fence_barrier_init();
+        S.abort = 0;
+        S.last = 0;
+        // the epoch moves only after every CTA of this launch has left, so all CTAs read one value
+        S.tag = *reinterpret_cast<volatile unsigned*>(&P.hdr->epoch) + 1u;
+    }
+    __syncthreads();
+    const uint32_t tag = S.tag;
+    const uint64_t limit = fused::g_wait_limit_ns;
+
+    if (warp == 0) {
+        if (lane == 0) producer<DT>(P, S, ring, tag, limit);
+        __syncwarp();
+    } else if (warp == 1) {
+        rproducer(P, S, rbuf, tag, limit);
+    } else if (warp < 2 + kQWarps) {
+        quantiser<DT>(P, S, ring, tag, limit, tid - 64);
+    } else {
+        reducer(P, S, rbuf, limit, tid - 64 - kQThreads);
+    }
+    __syncthreads();
+
+    if (tid == 0) {
+        // after an abort some copies may not have been waited for: let them land first
+        for (int s = 0; s < kSlots; ++s)
+            if (S.issued[s]) mbar_wait_bounded(&S.full[s], (S.issued[s] - 1u) & 1u, limit);
+        for (int b = 0; b < 2; ++b)
+            if (S.rissued[b]) mbar_wait_bounded(&S.rfull[b], (S.rissued[b] - 1u) & 1u, limit);
+        __threadfence();
+        S.last = atomicAdd(&P.hdr->exit_count, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (S.last) {
+        // the last CTA out resets the counters and advances the epoch for the next launch
+        if (tag == 0xffffffffu) {
+            // the tag space wrapped: clear every word so no old tag can match a later launch
+            for (size_t i = tid; i < P.tag_words; i += blockDim.x) P.tags[i] = 0;
+            __syncthreads();
+        }
+        if (tid == 0) {
+            P.hdr->q_head = 0;
+            P.hdr->r_head = 0;
+            P.hdr->exit_count = 0;
+            P.hdr->epoch = tag == 0xffffffffu ? 0u : tag;
+            __threadfence();
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------- host side
+
+struct PipeInit {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int ctas = 0;  // resident CTAs on this device
+};
+
+template <int DT>
+inline void init_pipe(PipeInit* pi) {
+    int per_sm = 0, sms = 0, dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_pipe<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_pipe<DT>, kThreads, kSmemBytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        pi->err = e;
+        pi->ctas = 0;
+        return;
+    }
+    pi->ctas = per_sm * sms;
+    if (pi->ctas <= 0) pi->err = cudaErrorNotSupported;
+}
+
+// Launches k_pipe over a workspace of at least workspace_bytes(W, rank_stride, num_chunks) bytes,
+// 256-byte aligned, zero-filled before its first launch.
+template <int DT>
+inline cudaError_t launch_pipe_dt(PipeInit* table, const QuantArgs& a, int order, float* out, int8_t* codes,
+                                  float* scales, void* ws, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    PipeInit& pi = table[dev];
+    std::call_once(pi.once, [&] { init_pipe<DT>(&pi); });
+    if (pi.err != cudaSuccess) return pi.err;
+    PArgs P;
+    P.q = a;
+    P.order = order;
+    P.out = out;
+    P.codes_out = codes;
+    P.scales_out = scales;
+    P.invW = 1.0f / static_cast<float>(a.W);
+    P.w_pow2 = (a.W & (a.W - 1)) == 0 ? 1 : 0;
+    P.neg_zero = -0.0f;
+    char* base = static_cast<char*>(ws);
+    P.hdr = reinterpret_cast<Hdr*>(base);
+    P.tags = reinterpret_cast<uint64_t*>(base + kHdrBytes);
+    P.tag_words = tag_region_bytes(a.num_chunks, a.W) / 8;
+    P.wcodes = reinterpret_cast<int8_t*>(base + kHdrBytes + tag_region_bytes(a.num_chunks, a.W));
+    P.cstride = code_stride(a.rank_stride);
+    P.total_q = static_cast<unsigned long long>(a.num_chunks) * static_cast<unsigned long long>(a.W);
+    P.total_r = P.total_q;
+    const unsigned long long want = P.total_q;
+    const unsigned grid = static_cast<unsigned>(want < static_cast<unsigned long long>(pi.ctas) ? want : pi.ctas);
+    k_pipe<DT><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace pipe
+}  // namespace gq

@@ -198,6 +198,36 @@ gq_status gq_fused_allreduce_sim_ws(const void* d_grads, gq_dtype dt, int W, siz
                                     float* d_scales_opt, void* d_workspace, size_t workspace_bytes,
                                     gq_stream_t stream);
 
+/* Bytes of device workspace gq_fused_allreduce_sim_pipelined needs: a 256-byte header, one 8-byte word
+ * per (chunk, rank), and W rows of int8 codes of rank_stride rounded up to 128 bytes (for the 25 MiB
+ * fp32 bucket at W = 8: 52.4 MB, a quarter of the gradients it covers). */
+size_t gq_pipelined_workspace_bytes(int W, size_t rank_stride, size_t num_chunks);
+
+/* gq_fused_allreduce_sim as the two-stage pipeline of the "pipelined HCCL AllReduce" article (§2.1:
+ * quantise chunk N+1 while chunk N is allreduced), one persistent CTA per SM running both stages:
+ *   - quantise stage, per (rank, chunk): the rank-chunk is bulk-copied (TMA, 16 KiB pieces) into a
+ *     ring of shared-memory slots, its absmax taken there, then it is quantised from shared memory;
+ *     the codes go to the workspace, where they stay in L2, and one word publishes the scale;
+ *   - reduce stage, per (chunk, ring segment): once the chunk's W scales are published (a wait bounded
+ *     in time), the segment's codes are read back from L2, dequantised, summed in the order, averaged
+ *     and stored, and their L2 lines dropped without a write-back.
+ * HBM traffic is the gradients read once and the output written once.  Same arguments, results (bit
+ * for bit) and errors as gq_fused_allreduce_sim, plus
+ *   d_found_inf_opt  NULL, or a device float set to 1.0f when an input value is Inf or NaN or
+ *                    overflows when unscaled (as gq_fused_allreduce_sim_amp)
+ *   d_workspace      device memory of at least gq_pipelined_workspace_bytes(W, rank_stride,
+ *                    num_chunks) bytes, 256-byte aligned, ZERO-FILLED before its first use.  It
+ *                    carries state from call to call (two work counters, reset by each call as it
+ *                    ends, and a launch counter that tags the published words): pass it unchanged to
+ *                    the next call.  After GQ_ERR_TIMEOUT zero-fill it again.  Calls that share a
+ *                    workspace must not overlap on the device (one stream, or one workspace each).
+ *   workspace_bytes  its size; GQ_ERR_INVALID_ARG if it is short. */
+gq_status gq_fused_allreduce_sim_pipelined(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                           const int64_t* d_offsets, size_t num_chunks, float loss_scale,
+                                           gq_order order, float* d_out, int8_t* d_codes_opt, float* d_scales_opt,
+                                           float* d_found_inf_opt, void* d_workspace, size_t workspace_bytes,
+                                           gq_stream_t stream);
+
 /* Bytes of the library's own device scratch array used by gq_fused_allreduce_sim_static: 1 MiB,
  * enough for chunk tables of up to 511 chunks at W = 8 (buckets of up to 64 MiB of fp32, or
  * 128 MiB of fp16, per rank under dynamic_chunk). */

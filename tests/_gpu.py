@@ -64,18 +64,32 @@ def run(host_rows, W, stride, bucket_elems, order, loss_scale=1.0, mode="fused",
         for _ in range(2):  # a second call on the same workspace: it must have been left zeroed
             gq.gq_fused_allreduce_sim_ws(grads, W, stride, d_off, nc, loss_scale, order, out, ws,
                                          codes if want_codes else None, scales if want_codes else None)
+    elif mode == "pipe":
+        ws = torch.zeros(gq.gq_pipelined_workspace_bytes(W, stride, nc), dtype=torch.uint8, device=dev)
+        for _ in range(2):  # a second call on the same workspace: counters reset, epoch advanced
+            gq.gq_fused_allreduce_sim_pipelined(grads, W, stride, d_off, nc, loss_scale, order, out, ws,
+                                                codes if want_codes else None, scales if want_codes else None)
     else:
         gq.gq_quantize(grads, W, stride, d_off, nc, loss_scale, codes, scales)
         gq.gq_reduce_dequant(codes, scales, W, stride, d_off, nc, order, out)
     status = gq.gq_get_error()
-    if ws is not None:
+    if ws is not None and mode == "fused_ws":
         # the queue head and exit count are back at zero for the next call
         assert int(ws[0].item()) == 0 and int(ws[1].item()) == 0, "workspace header not reset"
+    if ws is not None and mode == "pipe":
+        assert pipe_header(ws) == (0, 0, 0, 2), "workspace header after two calls: %r" % (pipe_header(ws),)
     assert guards_intact(out_buf, n_out), "write outside the output buffer"
     assert guards_intact(codes_buf, W * stride), "write outside the codes buffer"
     assert guards_intact(scales_buf, W * nc), "write outside the scales buffer"
     return (out.cpu().numpy(), codes.cpu().numpy(), scales.cpu().numpy().reshape(W, nc),
             d_off.cpu().numpy(), status)
+
+
+def pipe_header(ws):
+    """(quantise counter, reduce counter, exit count, launch epoch) of a pipelined workspace."""
+    h = ws[:24].cpu().numpy()
+    return (int(h[0:8].view(np.uint64)[0]), int(h[8:16].view(np.uint64)[0]), int(h[16:20].view(np.uint32)[0]),
+            int(h[20:24].view(np.uint32)[0]))
 
 
 def assert_bits_equal(got, want, what):

@@ -132,3 +132,40 @@ def test_plan_buckets_capacity_short(gq):
     assert L.gq_plan_buckets(te, 3, 4, 25 << 20, None, be, 2, ctypes.byref(nb)) == gq.GQ_ERR_INVALID_ARG
     assert nb.value == 3
     assert L.gq_plan_buckets(te, 3, 3, 25 << 20, None, be, 2, ctypes.byref(nb)) == gq.GQ_ERR_INVALID_ARG
+
+
+def _call_pipe(gq, grads=0x10000, dt=0, W=8, stride=1024, offsets=0x20000, nc=4, ls=1.0, order=1, out=0x30000,
+               codes=None, scales=None, found_inf=None, ws=0x100000, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = gq.gq_pipelined_workspace_bytes(W, stride, nc)
+    return gq.lib.gq_fused_allreduce_sim_pipelined(grads, dt, W, stride, offsets, nc, ls, order, out, codes, scales,
+                                                   found_inf, ws, ws_bytes, None)
+
+
+def test_pipelined_workspace_bytes(gq):
+    # 256-byte header, 8 bytes per (chunk, rank) rounded up to 256, W code rows of rank_stride
+    # rounded up to 128 bytes
+    assert gq.gq_pipelined_workspace_bytes(8, 6553600, 200) == 256 + 12800 + 8 * 6553600
+    assert gq.gq_pipelined_workspace_bytes(8, 1024, 4) == 256 + 256 + 8 * 1024
+    assert gq.gq_pipelined_workspace_bytes(3, 1001, 1) == 256 + 256 + 3 * 1024
+    assert gq.gq_pipelined_workspace_bytes(64, 128, 33) == 256 + 33 * 64 * 8 + 64 * 128
+
+
+def test_pipelined_rejects_bad_arguments(gq):
+    BAD, MIS = gq.GQ_ERR_INVALID_ARG, gq.GQ_ERR_MISALIGNED
+    assert _call_pipe(gq, grads=None) == BAD
+    assert _call_pipe(gq, out=None) == BAD
+    assert _call_pipe(gq, ws=None) == BAD
+    assert _call_pipe(gq, W=0) == BAD
+    assert _call_pipe(gq, W=65) == BAD
+    assert _call_pipe(gq, order=3) == BAD
+    assert _call_pipe(gq, ls=0.0) == BAD
+    need = gq.gq_pipelined_workspace_bytes(8, 1024, 4)
+    assert _call_pipe(gq, ws_bytes=need - 1) == BAD
+    assert _call_pipe(gq, ws=0x100080) == MIS           # workspace must be 256-byte aligned
+    assert _call_pipe(gq, found_inf=0x90002) == MIS
+    assert _call_pipe(gq, stride=1022) == MIS
+    # the workspace overlaps the gradient rows, the output or the found-inf word
+    assert _call_pipe(gq, ws=0x10100) == BAD
+    assert _call_pipe(gq, ws=0x30000 - 256) == BAD
+    assert _call_pipe(gq, found_inf=0x100100) == BAD

@@ -32,7 +32,7 @@ def _rows(cfg, W, n):
 # ------------------------------------------------------------------ workload 1 (small, full)
 
 @pytest.mark.parametrize("order,oorder", ORDERS)
-@pytest.mark.parametrize("mode", ["fused", "two_kernel"])
+@pytest.mark.parametrize("mode", ["fused", "two_kernel", "pipe"])
 def test_workload1_full(order, oorder, mode):
     W, n = 2, 262144
     host, stride = _rows(1, W, n)
@@ -45,7 +45,7 @@ def test_workload1_full(order, oorder, mode):
 # ------------------------------------------------------------------ workload 2 (headline, full)
 
 @pytest.mark.parametrize("order,oorder", ORDERS)
-@pytest.mark.parametrize("mode", ["fused", "fused_ws"])
+@pytest.mark.parametrize("mode", ["fused", "fused_ws", "pipe"])
 def test_workload2_full_fused(order, oorder, mode):
     W, n = 8, 6553600
     host, stride = _rows(2, W, n)
@@ -62,7 +62,7 @@ def test_workload2_two_kernel_ring():
     H.compare_full(host, W, stride, off, oracle.RING, 1.0, out, codes, scales)
 
 
-@pytest.mark.parametrize("mode", ["fused", "fused_ws"])
+@pytest.mark.parametrize("mode", ["fused", "fused_ws", "pipe"])
 def test_workload2_without_codes_output_is_deterministic(mode):
     """The timed configuration (no codes / scales written), three runs: identical bits."""
     W, n = 8, 6553600
@@ -88,7 +88,7 @@ def test_tree_within_tolerance_of_seq():
 
 # ------------------------------------------------------------------ workload 3 (ResNet-152 list)
 
-@pytest.mark.parametrize("mode", ["fused", "fused_ws"])
+@pytest.mark.parametrize("mode", ["fused", "fused_ws", "pipe"])
 def test_workload3_buckets_and_full_ring(mode):
     W = 8
     sizes, _ = wl.tensor_layout(3)
@@ -162,7 +162,7 @@ def test_fp16_unscale_full_small():
         wl.fill(4, r, 0, n, host[r * stride:r * stride + n])
     for ls in (65536.0, 3.0):
         for order, oorder in ORDERS[:2]:
-            for mode in ("fused", "two_kernel"):
+            for mode in ("fused", "two_kernel", "pipe"):
                 out, codes, scales, off, st = H.run(host, W, stride, [n], order, loss_scale=ls, mode=mode)
                 assert st == gq.GQ_OK
                 H.compare_full(host, W, stride, off, oorder, ls, out, codes, scales)
@@ -187,7 +187,7 @@ def test_workload5_sweep_full(n):
     W = 8
     host, stride, off = _sweep_rows(W, n)
     for order, oorder in ORDERS[:2]:
-        for mode in ("fused", "fused_ws"):
+        for mode in ("fused", "fused_ws", "pipe"):
             out, codes, scales, doff, st = H.run(host, W, stride, [n], order, mode=mode)
             assert st == gq.GQ_OK
             assert np.array_equal(doff, off)
@@ -224,7 +224,7 @@ def test_rank_counts(W):
     for r in range(W):
         wl.fill(1, r, 0, n, host[r * stride:r * stride + n])
     for order, oorder in ORDERS:
-        for mode in ("fused", "fused_ws", "two_kernel"):
+        for mode in ("fused", "fused_ws", "two_kernel", "pipe"):
             out, codes, scales, off, st = H.run(host, W, stride, [n], order, mode=mode)
             assert st == gq.GQ_OK
             H.compare_full(host, W, stride, off, oorder, 1.0, out, codes, scales)
@@ -242,17 +242,18 @@ def test_multi_bucket_ragged_table():
     for r in range(W):
         wl.fill(2, r, 0, n, host[r * stride:r * stride + n])
     for order, oorder in ORDERS:
-        for mode in ("fused", "fused_ws", "two_kernel"):
+        for mode in ("fused", "fused_ws", "two_kernel", "pipe"):
             out, codes, scales, off, st = H.run(host, W, stride, buckets, order, mode=mode)
             assert st == gq.GQ_OK
             assert np.array_equal(off, oracle.plan_chunks(buckets, 4))
             H.compare_full(host, W, stride, off, oorder, 1.0, out, codes, scales)
 
 
-def test_empty_bucket_only():
+@pytest.mark.parametrize("mode", ["fused", "pipe"])
+def test_empty_bucket_only(mode):
     W = 4
     host = np.zeros(W * 4, dtype=np.float32)
-    out, codes, scales, off, st = H.run(host, W, 4, [0], "ring")
+    out, codes, scales, off, st = H.run(host, W, 4, [0], "ring", mode=mode)
     assert st == gq.GQ_OK
     assert list(off) == [0, 0]
     assert np.all(scales == 0)
@@ -266,11 +267,12 @@ def test_constant_ranks_self_test():
     host = np.zeros(W * stride, dtype=np.float32)
     for r in range(W):
         host[r * stride:r * stride + n] = r + 1
-    out, codes, scales, off, st = H.run(host, W, stride, [n], "ring", mode="fused_ws")
-    assert st == gq.GQ_OK
-    assert np.all(codes.reshape(W, stride)[:, :n] == 127)
-    assert np.all(np.abs(out[:n] - 4.5) <= 4 * np.spacing(np.float32(4.5)))
-    H.compare_full(host, W, stride, off, oracle.RING, 1.0, out, codes, scales)
+    for mode in ("fused_ws", "pipe"):
+        out, codes, scales, off, st = H.run(host, W, stride, [n], "ring", mode=mode)
+        assert st == gq.GQ_OK
+        assert np.all(codes.reshape(W, stride)[:, :n] == 127)
+        assert np.all(np.abs(out[:n] - 4.5) <= 4 * np.spacing(np.float32(4.5)))
+        H.compare_full(host, W, stride, off, oracle.RING, 1.0, out, codes, scales)
 
 
 def test_nonfinite_input_is_reported():
@@ -282,7 +284,7 @@ def test_nonfinite_input_is_reported():
     host[1 * stride + 5] = np.inf      # chunk 0 of rank 1
     host[3 * stride + 200000] = np.nan  # a later chunk of rank 3
     off = oracle.plan_chunks([n], 4)
-    for mode in ("fused", "two_kernel"):
+    for mode in ("fused", "two_kernel", "pipe"):
         out, codes, scales, _, st = H.run(host, W, stride, [n], "ring", mode=mode)
         assert st == gq.GQ_WARN_NONFINITE
         want, _, wscales, nf = oracle.fused(host, W, stride, off, oracle.RING)
@@ -319,7 +321,7 @@ def test_bad_chunk_table_is_reported_and_skipped():
     #         [3000,9000) past the row, [9000,-5) backwards, [-5,3500) negative, [3500,3600) ok
     table = np.array([0, 1000, 5000, 2000, 3000, 9000, -5, 3500, 3600], dtype=np.int64)
     good = [(0, 1000), (2000, 3000), (3500, 3600)]
-    for mode in ("fused", "two_kernel", "fused_ws"):
+    for mode in ("fused", "two_kernel", "fused_ws", "pipe"):
         for order, oorder in ORDERS:
             out, codes, scales, _, st = H.run(host, W, stride, None, order, mode=mode, offsets=table)
             assert st == gq.GQ_ERR_BAD_TABLE
@@ -361,7 +363,7 @@ def test_ws_large_unaligned_chunks(order, oorder):
     for r in range(W):
         wl.fill(2, r, 0, n, host[r * stride:r * stride + n])
     table = np.array([0, 3, 200003, 200010, 450001, 450001, 460000], dtype=np.int64)
-    for mode in ("fused_ws", "fused"):
+    for mode in ("fused_ws", "fused", "pipe"):
         out, codes, scales, _, st = H.run(host, W, stride, None, order, mode=mode, offsets=table)
         assert st == gq.GQ_OK
         H.compare_full(host, W, stride, table, oorder, 1.0, out[:n], codes, scales)
