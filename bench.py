@@ -4,7 +4,8 @@ Workload: W = 8 virtual ranks, one flat 25 MiB fp32 DDP bucket (6,553,600 elemen
 rank, Laplace(0, 1e-4) values with 30% exact zeros and 0.1% outliers x100, dynamic_chunk
 into 200 chunks of 32,768, ring-order int8 dequantise-sum, mean.  A step is one pass of the
 whole path: the chunk table (gq_plan_chunks) and the fused quantise + reduce
-(gq_fused_allreduce_sim, or gq_fused_allreduce_sim_ws with --entry ws) over one input set.  Steps rotate over input sets whose total is
+(gq_fused_allreduce_sim_pipelined by default; gq_fused_allreduce_sim with --entry plain,
+gq_fused_allreduce_sim_ws with --entry ws) over one input set.  Steps rotate over input sets whose total is
 several times the 129 MB L2, so every step reads its gradients from HBM.
 
 Metric: input GB/s = W * n * 4 bytes per step / step time (the fused kernel also writes
@@ -47,7 +48,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length (cpu_baseline)")
-    p.add_argument("--entry", default="plain", choices=["ws", "plain", "pipe"],
+    p.add_argument("--entry", default="pipe", choices=["ws", "plain", "pipe"],
                    help="ws: gq_fused_allreduce_sim_ws (work-queue kernel); plain: gq_fused_allreduce_sim; "
                         "pipe: gq_fused_allreduce_sim_pipelined")
     return p.parse_args()

@@ -75,6 +75,10 @@ constexpr int kWarpsPerPiece = 2;
 constexpr int kPairs = kQWarps / kWarpsPerPiece;
 constexpr int kHalfGroups = kGroupsPerPiece / kWarpsPerPiece;  // groups per warp per piece
 constexpr int kGroupsPerLane = kHalfGroups / 32;
+#ifndef GQ_PIPE_UNROLL_B
+#define GQ_PIPE_UNROLL_B 4
+#endif
+constexpr int kUnrollB = GQ_PIPE_UNROLL_B;  // groups of the quantise pass a lane has in flight
 static_assert(kQWarps % kWarpsPerPiece == 0 && kHalfGroups % 32 == 0, "piece split");
 // Items of at least this many pieces are copied twice (absmax pass, then quantise pass, the second
 // from L2) instead of being held in the ring whole; above kSlots pieces they must be.
@@ -557,7 +561,7 @@ __device__ void quantiser(const PArgs& P, Shared& S, const unsigned char* ring, 
             const unsigned char* base = ring + static_cast<size_t>(slot) * kPiece + half * (kHalfGroups * 16);
             if (ng == kHalfGroups && gp - gf0 < gfull && gp + ng <= gf0 + gfull && !urow) {
                 // a full half-piece of whole groups, codes to the workspace only
-#pragma unroll 4
+#pragma unroll kUnrollB
                 for (int k = 0; k < kGroupsPerLane; ++k) {
                     const uint32_t gl = lane + 32 * k;
                     const V16 v = ld_shared_v16(base + gl * 16);
