@@ -14,6 +14,12 @@ from . import build as _build
 
 F32, F16 = 0, 1
 SEQ, RING, TREE = 0, 1, 2
+HIER_BASE = 0x100
+
+
+def HIER(L):
+    """Order code of the hierarchical order with nodes of L ranks (same encoding as gq.h)."""
+    return HIER_BASE + int(L)
 
 _lib = None
 
@@ -34,6 +40,8 @@ def lib():
         L.oracle_quantize.restype = i64
         L.oracle_reduce.argtypes = [p, p, ctypes.c_int, i64, p, i64, ctypes.c_int, p]
         L.oracle_reduce.restype = None
+        L.oracle_reduce_hier.argtypes = [p, p, ctypes.c_int, i64, p, i64, ctypes.c_int, p]
+        L.oracle_reduce_hier.restype = ctypes.c_int
         L.oracle_amp_update_scale.argtypes = [p, p, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_int32]
         L.oracle_amp_update_scale.restype = None
         L.oracle_half_to_float.argtypes = [ctypes.c_uint16]
@@ -104,6 +112,12 @@ def reduce(codes, scales, W, rank_stride, offsets, order):
     nc = len(off) - 1
     assert s.size == W * nc and c.size >= W * rank_stride
     out = np.zeros(int(off[-1]), dtype=np.float32)
+    if order > HIER_BASE:
+        rc = lib().oracle_reduce_hier(_ptr(c), _ptr(s), int(W), int(rank_stride), _ptr(off), nc,
+                                      int(order) - HIER_BASE, _ptr(out))
+        if rc != 0:
+            raise ValueError("node size %d does not divide W = %d" % (order - HIER_BASE, W))
+        return out
     lib().oracle_reduce(_ptr(c), _ptr(s), int(W), int(rank_stride), _ptr(off), nc, int(order), _ptr(out))
     return out
 

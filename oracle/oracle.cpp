@@ -182,6 +182,42 @@ void oracle_reduce(const int8_t* codes, const float* scales, int W, int64_t rank
     }
 }
 
+int oracle_reduce_hier(const int8_t* codes, const float* scales, int W, int64_t rank_stride,
+                       const int64_t* offsets, int64_t num_chunks, int L, float* out) {
+    if (L < 1 || W % L != 0) return -1;
+    if (!round_to_nearest_mode()) std::fesetround(FE_TONEAREST);
+    const int nodes = W / L;
+    std::vector<float> d(W);
+    for (int64_t j = 0; j < num_chunks; ++j) {
+        const int64_t lo = offsets[j], hi = offsets[j + 1];
+        const int64_t len = hi - lo;
+        const int64_t seg = (len + L - 1) / L;  // torch.chunk(chunk, L) piece length
+        for (int64_t i = lo; i < hi; ++i) {
+            for (int r = 0; r < W; ++r) {
+                const float q = static_cast<float>(codes[static_cast<int64_t>(r) * rank_stride + i]);
+                d[r] = q * scales[static_cast<int64_t>(r) * num_chunks + j];
+            }
+            // stage 1: ring inside each node over the node's own segment schedule
+            const int t = static_cast<int>((i - lo) / seg);
+            std::vector<float> level(nodes);
+            for (int n = 0; n < nodes; ++n) {
+                float node_sum = d[n * L + (t + 1) % L];
+                for (int k = 2; k <= L; ++k) node_sum = node_sum + d[n * L + (t + k) % L];
+                level[n] = node_sum;
+            }
+            // stage 2: aggregation tree over the node sums
+            while (level.size() > 1) {
+                std::vector<float> next;
+                for (size_t p = 0; p + 1 < level.size(); p += 2) next.push_back(level[p] + level[p + 1]);
+                if (level.size() % 2 == 1) next.push_back(level.back());
+                level.swap(next);
+            }
+            out[i] = level[0] / static_cast<float>(W);
+        }
+    }
+    return 0;
+}
+
 void oracle_amp_update_scale(float* scale, int32_t* tracker, float found_inf, float growth, float backoff,
                              int32_t interval) {
     if (found_inf != 0.0f) {  // true for NaN as well

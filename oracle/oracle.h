@@ -82,6 +82,18 @@ int64_t oracle_quantize(const void* grads, int dt, int W, int64_t rank_stride,
 void oracle_reduce(const int8_t* codes, const float* scales, int W, int64_t rank_stride,
                    const int64_t* offsets, int64_t num_chunks, int order, float* out);
 
+/* The same arithmetic in the hierarchical (topology-aware) order ([HCCL-PIPE] §2.1 third
+ * stage: a flat ring over all cards replaced by one ring inside each machine plus an
+ * aggregation tree between machines; §3.2 intra-machine groups and inter-machine tree).
+ * The W ranks form W / L nodes of L consecutive ranks (node n = ranks n*L .. n*L+L-1).
+ * For an element in segment t of torch.chunk(chunk, L), node n sums its ranks in ring
+ * order: local rank (t+1) % L first, then (t+2) % L, ..., t.  The W / L node sums are then
+ * added pairwise in node index order, an odd one carried up a level (the TREE rule over
+ * nodes); out = acc / (float)W.  L == W is the RING order and L == 1 the TREE order.
+ * Returns 0, or -1 (writing nothing) if L < 1 or W % L != 0. */
+int oracle_reduce_hier(const int8_t* codes, const float* scales, int W, int64_t rank_stride,
+                       const int64_t* offsets, int64_t num_chunks, int L, float* out);
+
 /* One step of the dynamic loss-scale update that follows the found-inf check in a mixed-precision
  * step ([HCCL-PIPE] §6.1 mixed precision; torch.cuda.amp.GradScaler.update semantics):
  *   found_inf != 0 (NaN counts as set): scale = (float)(scale * backoff), tracker = 0

@@ -98,5 +98,15 @@ def reduce_element(qs, ss, order, t):
     return rn32(frac(acc) / W)
 
 
+def reduce_element_hier(qs, ss, L, t):
+    """Mean over ranks in the hierarchical order: nodes of L consecutive ranks, each summed in
+    ring order from local rank (t+1) % L (t = segment in torch.chunk(chunk, L)), then the node
+    sums pairwise in node order, an odd one carried."""
+    W = len(qs)
+    d = [rn32(Fraction(int(q)) * frac(s)) for q, s in zip(qs, ss)]
+    nodes = [sum_in_order([d[n * L + (t + k) % L] for k in range(1, L + 1)]) for n in range(W // L)]
+    return rn32(frac(sum_tree(nodes)) / W)
+
+
 def bits(x):
     return int(np.array(x, dtype=np.float32).view(np.uint32))

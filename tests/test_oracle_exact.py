@@ -54,7 +54,7 @@ def _case(seed, W, kind):
     return grads, stride, off
 
 
-@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("W", [1, 2, 3, 4, 5, 6, 8, 12])
 @pytest.mark.parametrize("kind", KINDS + ["mixed"])
 def test_quantize_reduce_exact(orc, W, kind):
     for seed in range(3):
@@ -79,6 +79,16 @@ def test_quantize_reduce_exact(orc, W, kind):
                     ss = [scales[r, j] for r in range(W)]
                     want = X.reduce_element(qs, ss, order, t)
                     assert X.bits(out[i]) == X.bits(want), (order, j, i)
+        for L in [L for L in range(1, W + 1) if W % L == 0]:
+            out = orc.reduce(codes, scales, W, stride, off, orc.HIER(L))
+            for j in range(nc):
+                lo, hi = int(off[j]), int(off[j + 1])
+                for i in range(lo, hi):
+                    t = X.segment_of(i, lo, hi, L)
+                    qs = [codes[r * stride + i] for r in range(W)]
+                    ss = [scales[r, j] for r in range(W)]
+                    want = X.reduce_element_hier(qs, ss, L, t)
+                    assert X.bits(out[i]) == X.bits(want), (L, j, i)
 
 
 @pytest.mark.parametrize("loss_scale", [65536.0, 1024.0, 3.0, 1.0])

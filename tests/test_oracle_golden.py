@@ -50,6 +50,22 @@ def test_reduce_orders(orc):
         assert [int(x) for x in out.view(np.uint32)] == [G.f32_bits(t) for t in case[key]], key
 
 
+def test_reduce_hier(orc):
+    (name, case), = G.keyed_cases("reduce_hier.txt")
+    W = int(case["W"][0])
+    rows = [np.array([G.f32(t) for t in case["rank%d" % r]], dtype=np.float32) for r in range(W)]
+    n = len(rows[0])
+    grads = np.concatenate(rows)
+    off = np.array([int(t) for t in case["offsets"]], dtype=np.int64)
+    codes, scales, nf = orc.quantize(grads, W, n, off)
+    assert [int(x) for x in scales.reshape(-1).view(np.uint32)] == [G.f32_bits(t) for t in case["scales"]]
+    orders = [(orc.SEQ, "seq"), (orc.RING, "ring"), (orc.TREE, "tree")]
+    orders += [(orc.HIER(L), "hier%d" % L) for L in (1, 2, 3, 6)]
+    for order, key in orders:
+        out = orc.reduce(codes, scales, W, n, off, order)
+        assert [int(x) for x in out.view(np.uint32)] == [G.f32_bits(t) for t in case[key]], key
+
+
 def test_bucket_assignment(orc):
     for eb, tensors, buckets in G.bucket_cases():
         bot, be = orc.assign_buckets(tensors, eb)

@@ -77,6 +77,63 @@ def test_two_ranks_orders_agree(orc):
     assert np.array_equal(outs[0].view(np.uint32), outs[2].view(np.uint32))
 
 
+def test_hier_reduces_to_ring_and_tree(orc):
+    """Hierarchical order: one node of W ranks is the ring order, W one-rank nodes the tree
+    order, and nodes of two ranks the tree order too (a two-term sum does not depend on which
+    term comes first, and the node sums are the tree's first level)."""
+    for W in (2, 4, 6, 8, 12, 16):
+        n = 3 * 32768 + 4099
+        grads = _grads(17 + W, W, n, "laplace")
+        off = orc.plan_chunks([n], 4)
+        codes, scales, _ = orc.quantize(grads, W, n, off)
+        ring = orc.reduce(codes, scales, W, n, off, orc.RING).view(np.uint32)
+        tree = orc.reduce(codes, scales, W, n, off, orc.TREE).view(np.uint32)
+        assert np.array_equal(orc.reduce(codes, scales, W, n, off, orc.HIER(W)).view(np.uint32), ring)
+        assert np.array_equal(orc.reduce(codes, scales, W, n, off, orc.HIER(1)).view(np.uint32), tree)
+        assert np.array_equal(orc.reduce(codes, scales, W, n, off, orc.HIER(2)).view(np.uint32), tree)
+
+
+def test_hier_node_swap(orc):
+    """With two nodes the top level is one commutative add: swapping the nodes' data leaves
+    every output bit unchanged."""
+    W, L, n = 8, 4, 4 * 8192 + 5
+    grads = _grads(29, W, n, "laplace").reshape(W, n)
+    off = orc.plan_chunks([n], 4)
+    out = orc.fused(grads.reshape(-1), W, n, off, orc.HIER(L))[0]
+    swapped = np.concatenate([grads[L:], grads[:L]])
+    out2 = orc.fused(swapped.reshape(-1), W, n, off, orc.HIER(L))[0]
+    assert np.array_equal(out.view(np.uint32), out2.view(np.uint32))
+
+
+def test_hier_node_rotation_shifts_segments(orc):
+    """Node ring schedule: segment t starts at local rank (t+1) % L.  With every row constant,
+    rotating each node's ranks by one (new local k holds old local k+1) makes segment t add the
+    same terms in the order that segment t+1 used before, so the per-segment results shift by
+    one segment, bit for bit."""
+    W, L, n = 8, 4, 4 * 8192
+    rng = np.random.default_rng(29)
+    consts = (rng.standard_normal(W) * 10.0 ** rng.uniform(-4, 4, W)).astype(np.float32)
+    rows = np.repeat(consts[:, None], n, axis=1)
+    off = np.array([0, n], dtype=np.int64)
+    seg = n // L
+    a = orc.fused(rows.reshape(-1), W, n, off, orc.HIER(L))[0].view(np.uint32)
+    rot = np.concatenate([np.roll(rows[b * L:(b + 1) * L], -1, axis=0) for b in range(W // L)])
+    b = orc.fused(rot.reshape(-1), W, n, off, orc.HIER(L))[0].view(np.uint32)
+    per_seg = [a[t * seg] for t in range(L)]
+    assert len(set(per_seg)) > 1  # the orders really round differently on this data
+    for t in range(L):
+        assert np.all(a[t * seg:(t + 1) * seg] == per_seg[t])
+        assert np.all(b[t * seg:(t + 1) * seg] == per_seg[(t + 1) % L]), t
+
+
+def test_hier_rejects_nondividing_node_size(orc):
+    grads = _grads(3, 6, 100)
+    off = np.array([0, 100], dtype=np.int64)
+    codes, scales, _ = orc.quantize(grads, 6, 100, off)
+    with pytest.raises(ValueError):
+        orc.reduce(codes, scales, 6, 100, off, orc.HIER(4))
+
+
 def test_quantisation_error_against_unquantised_mean(orc):
     """Turning quantisation off changes the mean by at most (1/W) * sum_r s_r / 2 plus
     rounding of the W-term sum (the page's 'disable quantisation to check precision')."""

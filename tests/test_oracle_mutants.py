@@ -55,6 +55,16 @@ MUTANTS = {
     "amp_overflow_keeps_count": ("        *tracker = 0;\n        return;", "        return;"),
     "amp_growth_unguarded": ("if (std::isfinite(grown)) *scale = grown;", "*scale = grown;"),
     "amp_interval_late": ("if (t == interval) {", "if (t > interval) {"),
+    "hier_node_plain_order": ("float node_sum = d[n * L + (t + 1) % L];\n                for (int k = 2; k <= L; ++k) node_sum = node_sum + d[n * L + (t + k) % L];",
+                              "float node_sum = d[n * L];\n                for (int k = 1; k < L; ++k) node_sum = node_sum + d[n * L + k];"),
+    "hier_ring_start_at_t": ("float node_sum = d[n * L + (t + 1) % L];\n                for (int k = 2; k <= L; ++k)",
+                             "float node_sum = d[n * L + t % L];\n                for (int k = 1; k < L; ++k)"),
+    "hier_segments_over_W": ("const int64_t seg = (len + L - 1) / L;", "const int64_t seg = (len + W - 1) / W;"),
+    "hier_strided_nodes": ("node_sum = node_sum + d[n * L + (t + k) % L];",
+                           "node_sum = node_sum + d[n + nodes * ((t + k) % L)];"),
+    "hier_top_sequential": ("for (size_t p = 0; p + 1 < level.size(); p += 2) next.push_back(level[p] + level[p + 1]);\n                if (level.size() % 2 == 1) next.push_back(level.back());\n                level.swap(next);\n            }\n            out[i] = level[0]",
+                            "next.push_back(level[0] + level[1]);\n                for (size_t p = 2; p < level.size(); ++p) next.push_back(level[p]);\n                level.swap(next);\n            }\n            out[i] = level[0]"),
+    "hier_mean_over_nodes": ("out[i] = level[0] / static_cast<float>(W);", "out[i] = level[0] / static_cast<float>(nodes);"),
     "amp_nan_not_overflow": ("if (found_inf != 0.0f) {", "if (found_inf > 0.0f) {"),
 }
 
@@ -65,6 +75,7 @@ def _battery(orc):
         ("dynamic_chunk_sizes", lambda: TG.test_dynamic_chunk_sizes(orc)),
         ("unscale_f16", lambda: TG.test_unscale_f16(orc)),
         ("reduce_orders", lambda: TG.test_reduce_orders(orc)),
+        ("reduce_hier", lambda: TG.test_reduce_hier(orc)),
         ("bucket_assignment", lambda: TG.test_bucket_assignment(orc)),
         ("multi_bucket", lambda: TP.test_plan_multi_bucket_table(orc)),
         ("mean_div", lambda: TE.test_mean_division_nonpower_of_two(orc)),
@@ -75,7 +86,7 @@ def _battery(orc):
     ]
     for name, case in G.keyed_cases("quantize_cases.txt"):
         checks.append(("quantize:" + name, lambda c=case, n=name: TG.test_quantize_cases(orc, n, c)))
-    for W in (3, 4, 5):
+    for W in (3, 4, 5, 6, 8):
         for kind in ("mixed", "normal"):
             checks.append(("exact:%d:%s" % (W, kind), lambda W=W, k=kind: TE.test_quantize_reduce_exact(orc, W, k)))
     checks.append(("f16_exact", lambda: TE.test_f16_unscale_exact(orc, 3.0)))
