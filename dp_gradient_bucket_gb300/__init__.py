@@ -32,7 +32,22 @@ GQ_STATIC_SCRATCH_BYTES = 1 << 20
 
 GQ_F32, GQ_F16 = 0, 1
 GQ_ORDER_SEQ, GQ_ORDER_RING, GQ_ORDER_TREE = 0, 1, 2
+GQ_ORDER_HIER = 0x100
 ORDERS = {"seq": GQ_ORDER_SEQ, "ring": GQ_ORDER_RING, "tree": GQ_ORDER_TREE}
+
+
+def GQ_ORDER_HIER_NODES(L):
+    """The hierarchical order with nodes of L consecutive ranks (gq.h)."""
+    return GQ_ORDER_HIER + int(L)
+
+
+def _order(order):
+    """An order given as a gq_order value, "seq" / "ring" / "tree", or "hier<L>" (e.g. "hier4")."""
+    if isinstance(order, str):
+        if order.startswith("hier"):
+            return GQ_ORDER_HIER_NODES(int(order[4:]))
+        return ORDERS[order]
+    return int(order)
 GQ_MAX_RANKS = 64
 GQ_DEFAULT_BUCKET_CAP_BYTES = 25 * 1024 * 1024
 
@@ -157,14 +172,14 @@ def gq_quantize(grads, W, rank_stride, d_offsets, num_chunks, loss_scale, codes,
 
 def gq_reduce_dequant(codes, scales, W, rank_stride, d_offsets, num_chunks, order, out, stream=None):
     st = lib.gq_reduce_dequant(_dptr(codes), _dptr(scales), W, rank_stride, _dptr(d_offsets), num_chunks,
-                               ORDERS.get(order, order), _dptr(out), _stream(stream))
+                               _order(order), _dptr(out), _stream(stream))
     _check(st, "gq_reduce_dequant")
 
 
 def gq_fused_allreduce_sim(grads, W, rank_stride, d_offsets, num_chunks, loss_scale, order, out,
                            codes=None, scales=None, stream=None):
     st = lib.gq_fused_allreduce_sim(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
-                                    num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out),
+                                    num_chunks, loss_scale, _order(order), _dptr(out),
                                     _dptr(codes), _dptr(scales), _stream(stream))
     _check(st, "gq_fused_allreduce_sim")
 
@@ -179,7 +194,7 @@ def gq_fused_allreduce_sim_ws(grads, W, rank_stride, d_offsets, num_chunks, loss
     gq_fused_workspace_bytes(num_chunks, W) bytes, zero-filled before its first use and then passed
     unchanged from call to call (zero it again only after a GQ_ERR_TIMEOUT)."""
     st = lib.gq_fused_allreduce_sim_ws(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
-                                       num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out), _dptr(codes),
+                                       num_chunks, loss_scale, _order(order), _dptr(out), _dptr(codes),
                                        _dptr(scales), _dptr(workspace), workspace.numel() * workspace.element_size(),
                                        _stream(stream))
     _check(st, "gq_fused_allreduce_sim_ws")
@@ -196,7 +211,7 @@ def gq_fused_allreduce_sim_pipelined(grads, W, rank_stride, d_offsets, num_chunk
     aligned, zero-filled before its first use and then passed unchanged from call to call (zero it
     again only after a GQ_ERR_TIMEOUT); `found_inf` (optional) a one-element float32 CUDA tensor."""
     st = lib.gq_fused_allreduce_sim_pipelined(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
-                                              num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out),
+                                              num_chunks, loss_scale, _order(order), _dptr(out),
                                               _dptr(codes), _dptr(scales), _dptr(found_inf), _dptr(workspace),
                                               workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "gq_fused_allreduce_sim_pipelined")
@@ -208,7 +223,7 @@ def gq_fused_allreduce_sim_static(grads, W, rank_stride, d_offsets, num_chunks, 
     allocated); GQError(GQ_ERR_TOO_LARGE) when the table needs more than GQ_STATIC_SCRATCH_BYTES.
     Calls that overlap on the device race on the one scratch array: keep them on one stream."""
     st = lib.gq_fused_allreduce_sim_static(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
-                                           num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out),
+                                           num_chunks, loss_scale, _order(order), _dptr(out),
                                            _dptr(codes), _dptr(scales), _stream(stream))
     _check(st, "gq_fused_allreduce_sim_static")
 
@@ -218,7 +233,7 @@ def gq_fused_allreduce_sim_amp(grads, W, rank_stride, d_offsets, num_chunks, los
     """gq_fused_allreduce_sim that also sets the device float `found_inf` to 1.0 when an input value
     is Inf or NaN (or overflows when unscaled), leaving it alone otherwise."""
     st = lib.gq_fused_allreduce_sim_amp(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
-                                        num_chunks, loss_scale, ORDERS.get(order, order), _dptr(out), _dptr(codes),
+                                        num_chunks, loss_scale, _order(order), _dptr(out), _dptr(codes),
                                         _dptr(scales), _dptr(found_inf), _stream(stream))
     _check(st, "gq_fused_allreduce_sim_amp")
 

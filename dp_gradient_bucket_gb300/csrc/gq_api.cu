@@ -150,6 +150,14 @@ gq_status gq_plan_chunks(const size_t* bucket_elems, size_t num_buckets, size_t 
     return GQ_OK;
 }
 
+// 0: not an order; 1: SEQ, RING or TREE; 2: hierarchical with a node size that divides W.
+static int order_kind(gq_order order, int W) {
+    const int o = static_cast<int>(order);
+    if (o == GQ_ORDER_SEQ || o == GQ_ORDER_RING || o == GQ_ORDER_TREE) return 1;
+    const int L = o - static_cast<int>(GQ_ORDER_HIER);
+    return L >= 1 && L <= GQ_MAX_RANKS && W >= 1 && W % L == 0 ? 2 : 0;
+}
+
 gq_status gq_quantize(const void* d_grads, gq_dtype dt, int W, size_t rank_stride, const int64_t* d_offsets,
                       size_t num_chunks, float loss_scale, int8_t* d_codes, float* d_scales, gq_stream_t stream) {
     gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
@@ -170,7 +178,7 @@ gq_status gq_reduce_dequant(const int8_t* d_codes, const float* d_scales, int W,
                             gq_stream_t stream) {
     if (!d_codes || !d_scales || !d_offsets || !d_out) return GQ_ERR_INVALID_ARG;
     if (W < 1 || W > GQ_MAX_RANKS) return GQ_ERR_INVALID_ARG;
-    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (!order_kind(order, W)) return GQ_ERR_INVALID_ARG;
     if (num_chunks < 1 || num_chunks > static_cast<size_t>(INT_MAX)) return GQ_ERR_INVALID_ARG;
     if (rank_stride > (static_cast<size_t>(1) << 40)) return GQ_ERR_INVALID_ARG;
     if (!aligned(d_codes, 16) || !aligned(d_out, 16) || !aligned(d_scales, 4) || !aligned(d_offsets, 8))
@@ -191,7 +199,8 @@ gq_status gq_fused_allreduce_sim(const void* d_grads, gq_dtype dt, int W, size_t
     gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
     if (st != GQ_OK) return st;
     if (!d_out) return GQ_ERR_INVALID_ARG;
-    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (!order_kind(order, W)) return GQ_ERR_INVALID_ARG;
+    if (order_kind(order, W) == 2) return GQ_ERR_UNSUPPORTED;
     if (!aligned(d_out, 16) || (d_codes_opt && !aligned(d_codes_opt, 16)) ||
         (d_scales_opt && !aligned(d_scales_opt, 4)))
         return GQ_ERR_MISALIGNED;
@@ -214,7 +223,8 @@ gq_status gq_fused_allreduce_sim_amp(const void* d_grads, gq_dtype dt, int W, si
     gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
     if (st != GQ_OK) return st;
     if (!d_out || !d_found_inf) return GQ_ERR_INVALID_ARG;
-    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (!order_kind(order, W)) return GQ_ERR_INVALID_ARG;
+    if (order_kind(order, W) == 2) return GQ_ERR_UNSUPPORTED;
     if (!aligned(d_out, 16) || (d_codes_opt && !aligned(d_codes_opt, 16)) ||
         (d_scales_opt && !aligned(d_scales_opt, 4)) || !aligned(d_found_inf, 4))
         return GQ_ERR_MISALIGNED;
@@ -255,7 +265,8 @@ gq_status gq_fused_allreduce_sim_ws(const void* d_grads, gq_dtype dt, int W, siz
     gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
     if (st != GQ_OK) return st;
     if (!d_out || !d_workspace) return GQ_ERR_INVALID_ARG;
-    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (!order_kind(order, W)) return GQ_ERR_INVALID_ARG;
+    if (order_kind(order, W) == 2) return GQ_ERR_UNSUPPORTED;
     if (workspace_bytes < gq_fused_workspace_bytes(num_chunks, W)) return GQ_ERR_INVALID_ARG;
     if (!aligned(d_out, 16) || !aligned(d_workspace, 16) || (d_codes_opt && !aligned(d_codes_opt, 16)) ||
         (d_scales_opt && !aligned(d_scales_opt, 4)))
@@ -287,7 +298,7 @@ gq_status gq_fused_allreduce_sim_pipelined(const void* d_grads, gq_dtype dt, int
     gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
     if (st != GQ_OK) return st;
     if (!d_out || !d_workspace) return GQ_ERR_INVALID_ARG;
-    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (!order_kind(order, W)) return GQ_ERR_INVALID_ARG;
     if (workspace_bytes < gq_pipelined_workspace_bytes(W, rank_stride, num_chunks)) return GQ_ERR_INVALID_ARG;
     if (!aligned(d_out, 16) || !aligned(d_workspace, 256) || (d_codes_opt && !aligned(d_codes_opt, 16)) ||
         (d_scales_opt && !aligned(d_scales_opt, 4)) || (d_found_inf_opt && !aligned(d_found_inf_opt, 4)))
@@ -340,7 +351,8 @@ gq_status gq_fused_allreduce_sim_static(const void* d_grads, gq_dtype dt, int W,
     gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
     if (st != GQ_OK) return st;
     if (!d_out) return GQ_ERR_INVALID_ARG;
-    if (order != GQ_ORDER_SEQ && order != GQ_ORDER_RING && order != GQ_ORDER_TREE) return GQ_ERR_INVALID_ARG;
+    if (!order_kind(order, W)) return GQ_ERR_INVALID_ARG;
+    if (order_kind(order, W) == 2) return GQ_ERR_UNSUPPORTED;
     if (!aligned(d_out, 16) || (d_codes_opt && !aligned(d_codes_opt, 16)) ||
         (d_scales_opt && !aligned(d_scales_opt, 4)))
         return GQ_ERR_MISALIGNED;

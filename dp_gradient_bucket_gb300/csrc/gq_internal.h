@@ -13,6 +13,10 @@ constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrNonfinite = 2u;
 constexpr unsigned kErrBadTable = 4u;
 
+// Order codes as the kernels take them: 0 SEQ, 1 RING, 2 TREE, kOrderHierBase + L the
+// hierarchical order with nodes of L ranks (L divides W).
+constexpr int kOrderHierBase = 0x100;
+
 struct PlanBucket {  // one bucket of the chunk table, as kernel arguments
     int64_t elem_start;   // element offset of the bucket
     int64_t chunk_start;  // index of its first chunk in the table

@@ -215,6 +215,9 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const int8_t* codes, const 
     __syncthreads();
     if (hi == lo) return;
     const uint32_t seg = static_cast<uint32_t>((hi - lo + W - 1) / W);
+    // hierarchical order (0x100 + L): nodes of L ranks, segments of torch.chunk(chunk, L)
+    const int L = order > kOrderHierBase ? order - kOrderHierBase : 0;
+    const uint32_t segL = L > 0 ? static_cast<uint32_t>((hi - lo + L - 1) / L) : 1u;
     const int64_t g0 = lo / 4, g1 = (hi + 3) / 4, ng = g1 - g0;
     const int64_t per = (ng + gridDim.y - 1) / gridDim.y;
     const int64_t pg0 = g0 + min(ng, per * blockIdx.y), pg1 = g0 + min(ng, per * (blockIdx.y + 1));
@@ -230,7 +233,32 @@ __global__ void __launch_bounds__(kThreads) k_reduce(const int8_t* codes, const 
             for (int e = 0; e < 4; ++e) d[e] = __fmul_rn(code_to_float(w, e), s_scale[r]);
         };
         const int t0 = segment_of(first, lo, seg), t1 = segment_of(last, lo, seg);
-        if (order == 2) {
+        if (L > 0) {
+            // hierarchical: per element, a ring inside each node of L ranks over the segments of
+            // torch.chunk(chunk, L), then the node sums by the tree rule
+#pragma unroll 1
+            for (int e = 0; e < 4; ++e) {
+                const int64_t i = e0 + e;
+                acc[e] = 0.0f;
+                if (i < lo || i >= hi) continue;
+                const int t = segment_of(i, lo, segL);
+                const int rot = t + 1 == L ? 0 : t + 1;
+                TreeAcc tr;
+                tr.init();
+                for (int nb = 0; nb < W; nb += L) {
+                    int r = rot;
+                    float s = __fmul_rn(static_cast<float>(codes[static_cast<int64_t>(nb + r) * rank_stride + i]),
+                                        s_scale[nb + r]);
+                    for (int k = 1; k < L; ++k) {
+                        r = (r + 1 == L) ? 0 : r + 1;
+                        s = __fadd_rn(s, __fmul_rn(static_cast<float>(codes[static_cast<int64_t>(nb + r) * rank_stride + i]),
+                                                   s_scale[nb + r]));
+                    }
+                    tr.push(s);
+                }
+                acc[e] = tr.result();
+            }
+        } else if (order == 2) {
             TreeAcc tr[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) tr[e].init();

@@ -115,6 +115,8 @@ inline size_t workspace_bytes(int W, int64_t rank_stride, int64_t num_chunks) {
 struct PArgs {
     QuantArgs q;
     int order;
+    int hier_L;  // hierarchical order: ranks per node (0 under the other orders)
+    int nseg;    // reduce items per chunk: the segments of torch.chunk(chunk, nseg) (L, else W)
     float* out;
     int8_t* codes_out;  // [W][rank_stride], may be null
     float* scales_out;  // [W][num_chunks], may be null
@@ -148,7 +150,7 @@ struct Info {
 struct RInfo {
     int64_t a, b;  // elements of one ring segment
     int64_t c0;    // first code byte copied (16-byte aligned)
-    int rot;       // first rank of the summation order
+    int rot;       // first rank of the summation order (within a node under the hierarchical order)
     int valid;     // 0: no more units
     float s[kMaxRanks];  // the chunk's scales, by rank
 };
@@ -161,6 +163,7 @@ struct Shared {
     Info info[kInfo];
     RInfo rinfo[2];
     uint32_t issued[kSlots];  // phases started on full[] (to let copies land before exit)
+    uint32_t slot_seq[kSlots];  // the piece a slot was last taken for (~0 before its first)
     uint32_t rissued[2];
     uint32_t qmax[2][kQWarps];
     uint32_t tag;
@@ -208,6 +211,14 @@ __device__ __forceinline__ uint32_t ld_shared_u32(const void* p) {
     uint32_t v;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)));
     return v;
+}
+__device__ __forceinline__ uint32_t ld_acquire_shared_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_shared_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
 }
 
 // Packed pairs of binary32 (f32x2): each half rounds exactly as the scalar operation would.
@@ -289,6 +300,28 @@ __device__ __forceinline__ bool warp_wait_slot(uint64_t* bar, uint32_t parity, u
     return __all_sync(0xffffffffu, ok);
 }
 
+// Wait (whole warp) until piece s of the gradient ring has landed.  A parity wait cannot tell the
+// phase of piece s from that of piece s - 2 * kSlots, and bulk copies complete in any order, so a
+// warp that started waiting while piece s - kSlots of the same slot was still in flight would pass
+// at once.  The producer writes s into slot_seq only after piece s - kSlots was released (so had
+// landed): once slot_seq shows s, the slot's barrier is at most one phase short of piece s and the
+// parity wait is exact.
+__device__ __forceinline__ bool warp_wait_piece(Shared& S, uint32_t s, uint64_t limit_ns) {
+    const uint32_t slot = s % kSlots;
+    bool ok = true;
+    if (ld_acquire_shared_u32(&S.slot_seq[slot]) != s) {
+        const uint64_t t0 = global_timer_ns();
+        while (ld_acquire_shared_u32(&S.slot_seq[slot]) != s) {
+            if (ld_volatile_int(&S.abort) || global_timer_ns() - t0 > limit_ns) {
+                ok = false;
+                break;
+            }
+        }
+    }
+    ok = ok && wait_slot(&S.full[slot], (s / kSlots) & 1u, limit_ns, &S.abort);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ----------------------------------------------------------------------------- producer
 
 template <int DT>
@@ -353,6 +386,7 @@ __device__ void producer(const PArgs& P, Shared& S, unsigned char* ring, uint32_
                 const uint32_t slot = seq % kSlots;
                 const int64_t left = bytes - static_cast<int64_t>(p) * kPiece;
                 const uint32_t nb = static_cast<uint32_t>(left < kPiece ? left : kPiece);
+                st_release_shared_u32(&S.slot_seq[slot], seq);  // after the descriptor, before the arrival
                 mbar_arrive_expect_tx(&S.full[slot], nb + extra);
                 extra = 0;
                 bulk_copy_g2s_hint(ring + static_cast<size_t>(slot) * kPiece, src + static_cast<int64_t>(p) * kPiece, nb,
@@ -369,6 +403,7 @@ __device__ void producer(const PArgs& P, Shared& S, unsigned char* ring, uint32_
     if (ok && acquire(seq)) {
         const uint32_t slot = seq % kSlots;
         S.info[k % kInfo].valid = 0;
+        st_release_shared_u32(&S.slot_seq[slot], seq);
         mbar_arrive(&S.full[slot]);
         S.issued[slot] += 1u;
     }
@@ -451,7 +486,7 @@ __device__ void quantiser(const PArgs& P, Shared& S, const unsigned char* ring, 
 
     for (uint32_t k = 0;; ++k) {
         // ---- next item: its first piece has landed (or the end marker was posted)
-        const bool ok = !fail && warp_wait_slot(&S.full[cseq % kSlots], (cseq / kSlots) & 1u, limit, &S.abort);
+        const bool ok = !fail && warp_wait_piece(S, cseq, limit);
         Info in;
         in.valid = 0;
         if (ok) in = S.info[k % kInfo];
@@ -479,7 +514,7 @@ __device__ void quantiser(const PArgs& P, Shared& S, const unsigned char* ring, 
         for (int p = pair; p < in.np && !fail; p += kPairs) {
             const uint32_t s = cseq + static_cast<uint32_t>(p);
             const uint32_t slot = s % kSlots;
-            if (p > 0 && !warp_wait_slot(&S.full[slot], (s / kSlots) & 1u, limit, &S.abort)) {
+            if (p > 0 && !warp_wait_piece(S, s, limit)) {
                 fail = true;
                 break;
             }
@@ -552,7 +587,7 @@ __device__ void quantiser(const PArgs& P, Shared& S, const unsigned char* ring, 
         for (int p = pair; p < in.np && !fail; p += kPairs) {
             const uint32_t s = bseq + static_cast<uint32_t>(p);
             const uint32_t slot = s % kSlots;
-            if (in.twopass && !warp_wait_slot(&S.full[slot], (s / kSlots) & 1u, limit, &S.abort)) {
+            if (in.twopass && !warp_wait_piece(S, s, limit)) {
                 fail = true;
                 break;
             }
@@ -622,9 +657,10 @@ __device__ void quantiser(const PArgs& P, Shared& S, const unsigned char* ring, 
 static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf, uint32_t tag, uint64_t limit) {
     const int lane = threadIdx.x & 31;
     const int W = P.q.W;
-    const unsigned long long UW = static_cast<unsigned long long>(W);
+    const unsigned long long US = static_cast<unsigned long long>(P.nseg);
     const int64_t n = P.q.num_chunks;
     const bool ring = P.order == fused::kOrderRing;
+    const int L = P.hier_L;
     const int64_t E = r_unit(W);
     const uint32_t row = static_cast<uint32_t>(r_row(W));
     const uint64_t once = l2_policy_evict_first();
@@ -648,8 +684,8 @@ static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf,
     item = __shfl_sync(0xffffffffu, item, 0);
     for (;;) {
         if (item >= P.total_r || ld_volatile_int(&S.abort)) break;
-        const int64_t j = static_cast<int64_t>(item / UW);
-        const int t = static_cast<int>(item % UW);
+        const int64_t j = static_cast<int64_t>(item / US);
+        const int t = static_cast<int>(item % US);
         // claim the item after next now: its latency hides behind this one
         unsigned long long after = 0;
         if (lane == 0) after = atomicAdd(&P.hdr->r_head, 1ull);
@@ -657,7 +693,7 @@ static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf,
         next = after;
         int64_t lo, hi;
         if (!chunk_bounds(P.q.offsets, j, n, P.q.rank_stride, &lo, &hi) || hi == lo) continue;
-        const int64_t seg = (hi - lo + W - 1) / W;  // torch.chunk(chunk, W) piece length
+        const int64_t seg = (hi - lo + P.nseg - 1) / P.nseg;  // torch.chunk(chunk, nseg) piece length
         const int64_t a = min(hi, lo + static_cast<int64_t>(t) * seg), b = min(hi, a + seg);
         if (b <= a) continue;
         // the chunk's W words must carry this launch's tag (each is published after its codes)
@@ -691,7 +727,7 @@ static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf,
         }
         fence_acq_rel_gpu();         // acquire: the codes stored before the words
         fence_proxy_async_global();  // ... and before the bulk copies that read them
-        const int rot = ring ? (t + 1 == W ? 0 : t + 1) : 0;
+        const int rot = ring ? (t + 1 == W ? 0 : t + 1) : L > 0 ? (t + 1 == L ? 0 : t + 1) : 0;
         for (int64_t x = a; x < b; x += E) {
             if (!acquire(useq)) {
                 ok = false;
@@ -827,12 +863,92 @@ __device__ __forceinline__ void reduce_group16_tree(const PArgs& P, const unsign
     }
 }
 
-static __device__ void reducer(const PArgs& P, Shared& S, const unsigned char* rbuf, uint64_t limit, int rtid) {
+// TreeAcc on packed pairs: pairwise sums in push order, an odd one carried up a level, for up
+// to 127 pushes (a binary counter of partial sums; st[b] holds a sum of 2^b pushes).
+struct TreeAcc2 {
+    uint64_t st[7];
+    uint32_t count;
+    __device__ __forceinline__ void init() { count = 0; }
+    __device__ __forceinline__ void push(uint64_t x) {
+        uint32_t c = count;
+        int k = 0;
+#pragma unroll
+        for (int b = 0; b < 7; ++b) {
+            if (!(c & 1u)) break;
+            x = add2(st[b], x);
+            k = b + 1;
+            c >>= 1;
+        }
+#pragma unroll
+        for (int b = 0; b < 7; ++b)
+            if (b == k) st[b] = x;
+        ++count;
+    }
+    // the partial sums left, smallest first, each added to the running total
+    __device__ __forceinline__ uint64_t result() const {
+        uint64_t acc = 0;
+        bool have = false;
+#pragma unroll
+        for (int b = 0; b < 7; ++b) {
+            if ((count >> b) & 1u) {
+                acc = have ? add2(st[b], acc) : st[b];
+                have = true;
+            }
+        }
+        return acc;
+    }
+};
+
+// The same under the hierarchical order, two elements (one packed pair) at a time: per node of
+// L consecutive ranks, the node's ranks in ring order from local rank `rot`, then the node sums
+// by the tree rule.
+__device__ __forceinline__ void reduce_group16_hier(const PArgs& P, const unsigned char* base, uint32_t row,
+                                                   const float* sc, int W, int L, int rot, int64_t e0, int64_t c0,
+                                                   int64_t a, int64_t b, bool pow2) {
+    const uint64_t C2 = pk(kCodeBias, kCodeBias);
+    const uint64_t z2 = pk(P.neg_zero, P.neg_zero);
+#pragma unroll 1
+    for (int q = 0; q < 8; ++q) {
+        const int64_t f0 = e0 + 2 * q;
+        if (f0 + 2 <= a || f0 >= b) continue;
+        const uint32_t off = static_cast<uint32_t>(f0 - c0);
+        TreeAcc2 tr;
+        tr.init();
+        for (int nb = 0; nb < W; nb += L) {
+            uint64_t n0 = 0;
+            int r = rot;
+            for (int k = 0; k < L; ++k) {
+                const uint32_t wx = (ld_shared_u32(base + (nb + r) * row + (off & ~3u)) >> (8 * (off & 3u))) ^ 0x8080u;
+                const float s = sc[nb + r];
+                const uint64_t p0 = fma2(sub2(pk(code_biased(wx, 0), code_biased(wx, 1)), C2), pk(s, s), z2);
+                n0 = k == 0 ? p0 : add2(n0, p0);
+                r = r + 1 == L ? 0 : r + 1;
+            }
+            tr.push(n0);
+        }
+        float o0, o1;
+        unpk(tr.result(), o0, o1);
+        o0 = mean_of(o0, W, P.invW, pow2);
+        o1 = mean_of(o1, W, P.invW, pow2);
+        if (f0 >= a && f0 + 2 <= b) {
+            *reinterpret_cast<float2*>(P.out + f0) = make_float2(o0, o1);
+        } else {
+            if (f0 >= a && f0 < b) P.out[f0] = o0;
+            if (f0 + 1 >= a && f0 + 1 < b) P.out[f0 + 1] = o1;
+        }
+    }
+}
+
+// HIER: the hierarchical-order build of the kernel (its own register allocation); the other
+// build takes the sequential, ring and tree orders.
+template <bool HIER>
+__device__ void reducer(const PArgs& P, Shared& S, const unsigned char* rbuf, uint64_t limit, int rtid) {
     const int lane = rtid & 31;
     const int W = P.q.W;
     const uint32_t row = static_cast<uint32_t>(r_row(W));
     const bool pow2 = P.w_pow2 != 0;
     const bool tree = P.order == fused::kOrderTree;
+    const int L = P.hier_L;
     for (uint32_t useq = 0;; ++useq) {
         const uint32_t buf = useq & 1u;
         if (!warp_wait_slot(&S.rfull[buf], (useq >> 1) & 1u, limit, &S.abort)) {
@@ -849,7 +965,9 @@ static __device__ void reducer(const PArgs& P, Shared& S, const unsigned char* r
         const unsigned char* base = rbuf + buf * kRBufBytes;
         const int64_t G0 = a / 16, G1 = (b + 15) / 16;
         for (int64_t G = G0 + rtid; G < G1; G += kRThreads) {
-            if (tree)
+            if (HIER)
+                reduce_group16_hier(P, base, row, ri.s, W, L, rot, G * 16, c0, a, b, pow2);
+            else if (tree)
                 reduce_group16_tree(P, base, row, ri.s, W, G * 16, c0, a, b, pow2);
             else
                 reduce_group16(P, base, row, ri.s, W, rot, G * 16, c0, a, b, pow2);
@@ -867,7 +985,7 @@ static __device__ void reducer(const PArgs& P, Shared& S, const unsigned char* r
 
 // ----------------------------------------------------------------------------- kernel
 
-template <int DT>
+template <int DT, bool HIER>
 __global__ void __launch_bounds__(kThreads, 1) k_pipe(const PArgs P) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Shared S;
@@ -879,6 +997,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pipe(const PArgs P) {
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], kWarpsPerPiece);
             S.issued[s] = 0;
+            S.slot_seq[s] = 0xffffffffu;
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&S.rfull[b], 1);
@@ -903,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pipe(const PArgs P) {
     } else if (warp < 2 + kQWarps) {
         quantiser<DT>(P, S, ring, tag, limit, tid - 64);
     } else {
-        reducer(P, S, rbuf, limit, tid - 64 - kQThreads);
+        reducer<HIER>(P, S, rbuf, limit, tid - 64 - kQThreads);
     }
     __syncthreads();
 
@@ -939,7 +1058,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pipe(const PArgs P) {
 struct PipeInit {
     std::once_flag once;
     cudaError_t err = cudaSuccess;
-    int ctas = 0;  // resident CTAs on this device
+    int ctas = 0;  // resident CTAs on this device (the smaller count of the two builds)
 };
 
 template <int DT>
@@ -947,10 +1066,18 @@ inline void init_pipe(PipeInit* pi) {
     int per_sm = 0, sms = 0, dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int per_sm_h = 0;
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_pipe<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+        e = cudaFuncSetAttribute(k_pipe<DT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_pipe<DT>, kThreads, kSmemBytes);
+        e = cudaFuncSetAttribute(k_pipe<DT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_pipe<DT, false>, kThreads, kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_h, k_pipe<DT, true>, kThreads, kSmemBytes);
+    if (per_sm_h < per_sm) per_sm = per_sm_h;
     if (e != cudaSuccess) {
         cudaGetLastError();
         pi->err = e;
@@ -976,6 +1103,8 @@ inline cudaError_t launch_pipe_dt(PipeInit* table, const QuantArgs& a, int order
     PArgs P;
     P.q = a;
     P.order = order;
+    P.hier_L = order > kOrderHierBase ? order - kOrderHierBase : 0;
+    P.nseg = P.hier_L > 0 ? P.hier_L : a.W;
     P.out = out;
     P.codes_out = codes;
     P.scales_out = scales;
@@ -989,10 +1118,13 @@ inline cudaError_t launch_pipe_dt(PipeInit* table, const QuantArgs& a, int order
     P.wcodes = reinterpret_cast<int8_t*>(base + kHdrBytes + tag_region_bytes(a.num_chunks, a.W));
     P.cstride = code_stride(a.rank_stride);
     P.total_q = static_cast<unsigned long long>(a.num_chunks) * static_cast<unsigned long long>(a.W);
-    P.total_r = P.total_q;
+    P.total_r = static_cast<unsigned long long>(a.num_chunks) * static_cast<unsigned long long>(P.nseg);
     const unsigned long long want = P.total_q;
     const unsigned grid = static_cast<unsigned>(want < static_cast<unsigned long long>(pi.ctas) ? want : pi.ctas);
-    k_pipe<DT><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    if (P.hier_L > 0)
+        k_pipe<DT, true><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    else
+        k_pipe<DT, false><<<grid, kThreads, kSmemBytes, stream>>>(P);
     return cudaGetLastError();
 }
 

@@ -62,7 +62,8 @@ typedef enum {
     GQ_ERR_MISALIGNED = 2,  /* base pointer or row start not on a 16-byte boundary     */
     GQ_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, attribute, copy)    */
     GQ_ERR_TIMEOUT = 4,     /* a device-side bounded wait gave up (gq_get_error only)  */
-    GQ_ERR_UNSUPPORTED = 5, /* the device cannot run the kernel (not sm_103, no clusters) */
+    GQ_ERR_UNSUPPORTED = 5, /* the device cannot run the kernel (not sm_103, no clusters), or the
+                               call does not take the order (GQ_ORDER_HIER) */
     GQ_WARN_NONFINITE = 6,  /* an input value was Inf or NaN (gq_get_error only)       */
     GQ_ERR_BAD_TABLE = 7,   /* a chunk table broke the rules above (gq_get_error only) */
     GQ_ERR_TOO_LARGE = 8    /* the problem needs more scratch than the library's static array
@@ -80,7 +81,24 @@ typedef enum { GQ_F32 = 0, GQ_F16 = 1 } gq_dtype;
  *   TREE: pairwise over ranks in index order, (0+1), (2+3), ...; an odd one out is
  *         carried up a level unchanged; repeated until one value remains.
  * Each step is one binary32 addition acc = acc + d. */
-typedef enum { GQ_ORDER_SEQ = 0, GQ_ORDER_RING = 1, GQ_ORDER_TREE = 2 } gq_order;
+typedef enum {
+    GQ_ORDER_SEQ = 0,
+    GQ_ORDER_RING = 1,
+    GQ_ORDER_TREE = 2,
+    /* Hierarchical (topology-aware) order, the value GQ_ORDER_HIER + L for nodes of L ranks
+     * (GQ_ORDER_HIER_NODES(L); 1 <= L <= GQ_MAX_RANKS, L divides W, else GQ_ERR_INVALID_ARG).
+     * The pipelined-AllReduce article (§2.1, third stage; §3.2) replaces one ring over all cards
+     * by a ring inside each machine and an aggregation tree between machines.  Here: the W ranks
+     * form W / L nodes of L consecutive ranks (node n = ranks n*L .. n*L+L-1); an element in
+     * segment t of torch.chunk(chunk, L) is summed inside each node from local rank (t+1) % L,
+     * then (t+2) % L, ..., t; the W / L node sums are then added by the TREE rule over nodes.
+     * L == W gives the RING result and L == 1 (or L == 2) the TREE result, bit for bit.
+     * Taken by gq_reduce_dequant and gq_fused_allreduce_sim_pipelined; the other fused calls
+     * return GQ_ERR_UNSUPPORTED for it. */
+    GQ_ORDER_HIER = 0x100,
+    GQ_ORDER_HIER_LAST_ = 0x100 + 64
+} gq_order;
+#define GQ_ORDER_HIER_NODES(L) ((gq_order)(GQ_ORDER_HIER + (L)))
 
 #define GQ_MAX_RANKS 64
 #define GQ_DEFAULT_BUCKET_CAP_BYTES ((size_t)25 * 1024 * 1024)

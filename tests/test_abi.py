@@ -82,6 +82,10 @@ def test_fused_rejects_bad_arguments(gq):
     assert _call_fused(gq, W=65) == BAD
     assert _call_fused(gq, dt=2) == BAD
     assert _call_fused(gq, order=3) == BAD
+    assert _call_fused(gq, order=0x100) == BAD              # hierarchical with L = 0
+    assert _call_fused(gq, order=0x103) == BAD              # L = 3 does not divide W = 8
+    assert _call_fused(gq, order=0x100 + 65) == BAD
+    assert _call_fused(gq, order=0x104) == gq.GQ_ERR_UNSUPPORTED  # valid, not taken by this call
     assert _call_fused(gq, nc=0) == BAD
     assert _call_fused(gq, ls=0.0) == BAD
     assert _call_fused(gq, ls=-1.0) == BAD
@@ -107,6 +111,8 @@ def test_quantize_and_reduce_reject_bad_arguments(gq):
     assert L.gq_quantize(0x10000, 0, 8, 1024, 0x20000, 4, 1.0, 0x10400, 0x60000, None) == BAD
     assert L.gq_reduce_dequant(None, 0x1000, 8, 1024, 0x2000, 4, 1, 0x3000, None) == BAD
     assert L.gq_reduce_dequant(0x10000, 0x1000, 8, 1024, 0x2000, 4, 7, 0x30000, None) == BAD
+    assert L.gq_reduce_dequant(0x10000, 0x1000, 8, 1024, 0x2000, 4, 0x100 + 3, 0x30000, None) == BAD
+    assert L.gq_reduce_dequant(0x10000, 0x1000, 8, 1024, 0x2000, 4, 0x100 + 16, 0x30000, None) == BAD
     assert L.gq_reduce_dequant(0x10000, 0x1000, 8, 1022, 0x2000, 4, 1, 0x30000, None) == MIS
     assert L.gq_reduce_dequant(0x10000, 0x1000, 8, 1024, 0x2000, 4, 1, 0x10100, None) == BAD
 
@@ -159,6 +165,8 @@ def test_pipelined_rejects_bad_arguments(gq):
     assert _call_pipe(gq, W=0) == BAD
     assert _call_pipe(gq, W=65) == BAD
     assert _call_pipe(gq, order=3) == BAD
+    assert _call_pipe(gq, order=0x100) == BAD
+    assert _call_pipe(gq, order=0x100 + 5) == BAD   # L = 5 does not divide W = 8
     assert _call_pipe(gq, ls=0.0) == BAD
     need = gq.gq_pipelined_workspace_bytes(8, 1024, 4)
     assert _call_pipe(gq, ws_bytes=need - 1) == BAD

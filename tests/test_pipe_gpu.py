@@ -43,6 +43,31 @@ def test_pipe_chunks_larger_than_the_ring(W, order, oorder):
     H.compare_full(host, W, stride, table, oorder, 1.0, out[:n], codes, scales)
 
 
+@pytest.mark.parametrize("W,dt", [(64, np.float32), (48, np.float32), (64, np.float16)])
+def test_pipe_many_items_per_cta_with_two_pass_chunks(W, dt):
+    """Many rank-chunks per CTA, two-pass chunks (longer than the ring) between single-pass ones:
+    a quantiser warp may reach a ring slot while the slot's previous piece is still in flight (bulk
+    copies land in any order).  Each call on a fresh workspace, several calls."""
+    eb = np.dtype(dt).itemsize
+    big = (262144 - 4) // eb  # one chunk of 256 KiB less one element: copied once per pass
+    buckets = [5, 0, 1, big, 131075 * 4 // eb, 7, big, 32769 * 3 + 1, 3, 196608 // eb, big]
+    n = sum(buckets)
+    stride = gq.row_stride(n, eb)
+    host = np.zeros(W * stride, dtype=dt)
+    for r in range(W):
+        wl.fill(4 if dt == np.float16 else 2, r, 0, n, host[r * stride:r * stride + n])
+    ls = 65536.0 if dt == np.float16 else 1.0
+    want = None
+    for rep in range(4):
+        out, codes, scales, off, st = H.run(host, W, stride, buckets, "ring", loss_scale=ls, mode="pipe")
+        assert st == gq.GQ_OK, "call %d" % rep
+        if want is None:
+            H.compare_full(host, W, stride, off, oracle.RING, ls, out, codes, scales)
+            want = out.copy()
+        else:
+            H.assert_bits_equal(out, want, "output of call %d" % rep)
+
+
 @pytest.mark.parametrize("W", [8, 16])
 def test_pipe_fp16_unscale(W):
     """fp16 gradients with loss scales 65536 (exact unscale) and 3 (inexact), every order."""
