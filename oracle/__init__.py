@@ -34,6 +34,10 @@ def lib():
         L.oracle_bucket_chunks.restype = i64
         L.oracle_plan_chunks.argtypes = [p, i64, i64, p, i64]
         L.oracle_plan_chunks.restype = i64
+        L.oracle_bucket_chunks_sized.argtypes = [i64, i64, i64, p]
+        L.oracle_bucket_chunks_sized.restype = i64
+        L.oracle_plan_chunks_ex.argtypes = [p, i64, i64, ctypes.c_int, i64, p, i64]
+        L.oracle_plan_chunks_ex.restype = i64
         L.oracle_assign_buckets.argtypes = [p, i64, i64, i64, p, p, i64]
         L.oracle_assign_buckets.restype = i64
         L.oracle_quantize.argtypes = [p, ctypes.c_int, ctypes.c_int, i64, p, i64, ctypes.c_float, p, p]
@@ -59,6 +63,27 @@ def bucket_chunks(n, eb):
     c = ctypes.c_int64(0)
     k = lib().oracle_bucket_chunks(int(n), int(eb), ctypes.byref(c))
     return int(k), int(c.value)
+
+
+def bucket_chunks_sized(n, eb, chunk_size):
+    """(count, piece length) of dynamic_chunk with base chunk size chunk_size bytes."""
+    c = ctypes.c_int64(0)
+    k = lib().oracle_bucket_chunks_sized(int(n), int(eb), int(chunk_size), ctypes.byref(c))
+    return int(k), int(c.value)
+
+
+SCOPE_CHUNK, SCOPE_BUCKET, SCOPE_TENSOR = 0, 1, 2
+
+
+def plan_chunks_ex(elems, eb, scope=SCOPE_CHUNK, chunk_size=128 * 1024):
+    """int64 offsets[num_chunks + 1] for entries (buckets or tensors) laid end to end."""
+    be = np.ascontiguousarray(elems, dtype=np.int64)
+    total = lib().oracle_plan_chunks_ex(_ptr(be), len(be), int(eb), int(scope), int(chunk_size), None, 0)
+    if total < 0:
+        raise ValueError("bad plan arguments")
+    off = np.empty(total + 1, dtype=np.int64)
+    lib().oracle_plan_chunks_ex(_ptr(be), len(be), int(eb), int(scope), int(chunk_size), _ptr(off), len(off))
+    return off
 
 
 def plan_chunks(bucket_elems, eb):

@@ -52,9 +52,9 @@ float oracle_half_to_float(uint16_t h) {
     return static_cast<float>(sign ? -v : v);  // exact: every binary16 value is a binary32 value
 }
 
-int64_t oracle_bucket_chunks(int64_t n, int64_t eb, int64_t* chunk_elems) {
+int64_t oracle_bucket_chunks_sized(int64_t n, int64_t eb, int64_t chunk_size, int64_t* chunk_elems) {
     const int64_t nbytes = n * eb;
-    int64_t k = nbytes / (kChunkSize - kChunkSize % kAlignment);  // num_chunks before max(1, .)
+    int64_t k = nbytes / (chunk_size - chunk_size % kAlignment);  // num_chunks before max(1, .)
     if (k < 1) k = 1;
     if (n == 0) {                       // torch.chunk of an empty tensor: one empty piece
         if (chunk_elems) *chunk_elems = 0;
@@ -65,25 +65,43 @@ int64_t oracle_bucket_chunks(int64_t n, int64_t eb, int64_t* chunk_elems) {
     return (n + c - 1) / c;             // pieces actually returned: ceil(n / c)
 }
 
-int64_t oracle_plan_chunks(const int64_t* bucket_elems, int64_t num_buckets, int64_t eb,
-                           int64_t* offsets, int64_t capacity) {
+int64_t oracle_bucket_chunks(int64_t n, int64_t eb, int64_t* chunk_elems) {
+    return oracle_bucket_chunks_sized(n, eb, kChunkSize, chunk_elems);
+}
+
+// Chunks of one entry of a plan: dynamic_chunk pieces, or the whole entry as one chunk.
+static int64_t entry_chunks(int64_t n, int64_t eb, int scope, int64_t chunk_size, int64_t* chunk_elems) {
+    if (scope == ORACLE_SCOPE_CHUNK) return oracle_bucket_chunks_sized(n, eb, chunk_size, chunk_elems);
+    if (chunk_elems) *chunk_elems = n;  // one scale over the whole bucket or tensor
+    return 1;
+}
+
+int64_t oracle_plan_chunks_ex(const int64_t* elems, int64_t count, int64_t eb, int scope, int64_t chunk_size,
+                              int64_t* offsets, int64_t capacity) {
+    if (scope != ORACLE_SCOPE_CHUNK && scope != ORACLE_SCOPE_BUCKET && scope != ORACLE_SCOPE_TENSOR) return -1;
+    if (scope == ORACLE_SCOPE_CHUNK && chunk_size - chunk_size % kAlignment <= 0) return -1;
     int64_t total = 0;
-    for (int64_t b = 0; b < num_buckets; ++b) {
-        if (bucket_elems[b] < 0) return -1;
-        total += oracle_bucket_chunks(bucket_elems[b], eb, nullptr);
+    for (int64_t b = 0; b < count; ++b) {
+        if (elems[b] < 0) return -1;
+        total += entry_chunks(elems[b], eb, scope, chunk_size, nullptr);
     }
     if (offsets == nullptr || capacity < total + 1) return total;
     int64_t pos = 0;       // next table slot
-    int64_t start = 0;     // element offset of the current bucket
-    for (int64_t b = 0; b < num_buckets; ++b) {
-        const int64_t n = bucket_elems[b];
+    int64_t start = 0;     // element offset of the current entry
+    for (int64_t b = 0; b < count; ++b) {
+        const int64_t n = elems[b];
         int64_t c = 0;
-        const int64_t count = oracle_bucket_chunks(n, eb, &c);
-        for (int64_t j = 0; j < count; ++j) offsets[pos++] = start + j * c;
+        const int64_t pieces = entry_chunks(n, eb, scope, chunk_size, &c);
+        for (int64_t j = 0; j < pieces; ++j) offsets[pos++] = start + j * c;
         start += n;
     }
     offsets[pos] = start;
     return total;
+}
+
+int64_t oracle_plan_chunks(const int64_t* bucket_elems, int64_t num_buckets, int64_t eb,
+                           int64_t* offsets, int64_t capacity) {
+    return oracle_plan_chunks_ex(bucket_elems, num_buckets, eb, ORACLE_SCOPE_CHUNK, kChunkSize, offsets, capacity);
 }
 
 int64_t oracle_assign_buckets(const int64_t* tensor_elems, int64_t num_tensors, int64_t eb,

@@ -45,6 +45,23 @@ enum { ORACLE_SEQ = 0, ORACLE_RING = 1, ORACLE_TREE = 2 };
  * Returns the chunk count; *chunk_elems receives c (0 for n == 0). */
 int64_t oracle_bucket_chunks(int64_t n, int64_t eb, int64_t* chunk_elems);
 
+/* The same with the base chunk size as a parameter (the page's CHUNK_SIZE; [HCCL-PIPE] §4.2
+ * Config knobs, §2.1): k = max(1, nbytes // (chunk_size - chunk_size % 64)). */
+int64_t oracle_bucket_chunks_sized(int64_t n, int64_t eb, int64_t chunk_size, int64_t* chunk_elems);
+
+/* Scope of one quantisation scale.  CHUNK: dynamic_chunk pieces of every entry (entries are
+ * buckets), with chunk_size as the base size.  BUCKET / TENSOR: each entry (a bucket, or a
+ * tensor) is one chunk, so one scale covers it whole -- the page's quantize_gradient applied
+ * to the whole gradient it is given ([HCCL-PIPE] §2.2.1), per bucket or per tensor.  An empty
+ * entry is one empty chunk.  Entries are laid end to end. */
+enum { ORACLE_SCOPE_CHUNK = 0, ORACLE_SCOPE_BUCKET = 1, ORACLE_SCOPE_TENSOR = 2 };
+
+/* Chunk table of count entries under a scope (writes count-dependent num_chunks+1 offsets when
+ * capacity >= num_chunks+1).  Returns num_chunks, or -1 on a negative size, an unknown scope or
+ * (scope CHUNK) a chunk size whose 64-byte-aligned part is 0. */
+int64_t oracle_plan_chunks_ex(const int64_t* elems, int64_t count, int64_t eb, int scope, int64_t chunk_size,
+                              int64_t* offsets, int64_t capacity);
+
 /* Chunk table for buckets laid end to end.  Writes num_chunks+1 offsets when
  * capacity >= num_chunks+1 (else writes nothing).  Returns num_chunks, or -1 on a
  * negative size. */

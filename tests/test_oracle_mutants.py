@@ -43,7 +43,7 @@ MUTANTS = {
     "mean_missing": ("out[i] = acc / static_cast<float>(W);", "out[i] = acc;"),
     "scales_transposed": ("d[r] = q * scales[static_cast<int64_t>(r) * num_chunks + j];",
                           "d[r] = q * scales[j * W + r];"),
-    "chunk_divisor_minus_alignment": ("(kChunkSize - kChunkSize % kAlignment)", "(kChunkSize - kAlignment)"),
+    "chunk_divisor_minus_alignment": ("(chunk_size - chunk_size % kAlignment)", "(chunk_size - kAlignment)"),
     "chunk_count_is_k": ("return (n + c - 1) / c;             // pieces", "return k;             // pieces"),
     "chunk_len_floor": ("const int64_t c = (n + k - 1) / k;", "const int64_t c = n / k;"),
     "plan_missing_bucket_base": ("offsets[pos++] = start + j * c;", "offsets[pos++] = j * c;"),
@@ -65,6 +65,10 @@ MUTANTS = {
     "hier_top_sequential": ("for (size_t p = 0; p + 1 < level.size(); p += 2) next.push_back(level[p] + level[p + 1]);\n                if (level.size() % 2 == 1) next.push_back(level.back());\n                level.swap(next);\n            }\n            out[i] = level[0]",
                             "next.push_back(level[0] + level[1]);\n                for (size_t p = 2; p < level.size(); ++p) next.push_back(level[p]);\n                level.swap(next);\n            }\n            out[i] = level[0]"),
     "hier_mean_over_nodes": ("out[i] = level[0] / static_cast<float>(W);", "out[i] = level[0] / static_cast<float>(nodes);"),
+    "whole_scope_skips_empty": ("    if (chunk_elems) *chunk_elems = n;  // one scale over the whole bucket or tensor\n    return 1;",
+                                "    if (chunk_elems) *chunk_elems = n;  // one scale over the whole bucket or tensor\n    return n > 0 ? 1 : 0;"),
+    "sized_ignores_chunk_size": ("return oracle_bucket_chunks_sized(n, eb, chunk_size, chunk_elems);",
+                                 "return oracle_bucket_chunks_sized(n, eb, kChunkSize, chunk_elems);"),
     "amp_nan_not_overflow": ("if (found_inf != 0.0f) {", "if (found_inf > 0.0f) {"),
 }
 
@@ -78,6 +82,8 @@ def _battery(orc):
         ("reduce_hier", lambda: TG.test_reduce_hier(orc)),
         ("bucket_assignment", lambda: TG.test_bucket_assignment(orc)),
         ("multi_bucket", lambda: TP.test_plan_multi_bucket_table(orc)),
+        ("plan_scopes", lambda: TP.test_plan_whole_bucket_and_whole_tensor_scopes(orc)),
+        ("plan_sized", lambda: TP.test_plan_sized_matches_torch_chunk(orc)),
         ("mean_div", lambda: TE.test_mean_division_nonpower_of_two(orc)),
         ("half_decode", lambda: TE.test_half_decode_all_patterns(orc)),
         ("amp_golden", TA.test_update_sequence_golden),

@@ -86,3 +86,61 @@ def test_bucket_greedy_is_maximal(orc):
             if b + 1 < len(be):
                 nxt = next(s for s, k in zip(sizes, bot) if k == b + 1)
                 assert (be[b] + nxt) * eb > cap
+
+
+def _page_dynamic_chunk_sized(t, chunk_size):
+    """The page's dynamic_chunk with its CHUNK_SIZE knob set to chunk_size, on the real
+    torch.chunk (alignment 64 as on the page)."""
+    nbytes = t.numel() * t.element_size()
+    return torch.chunk(t, max(1, nbytes // (chunk_size - chunk_size % 64)))
+
+
+def test_plan_sized_matches_torch_chunk(orc):
+    """Other base chunk sizes, including ones that are not multiples of the 64-byte alignment
+    (so the page's `chunk_size - chunk_size % alignment` term matters)."""
+    rng = np.random.default_rng(21)
+    base = torch.empty(2 ** 22, dtype=torch.float32)
+    for chunk_size in (100, 4096, 16384, 32868, 65536, 131072, 262144, 1048576, 1000003):
+        sizes = sorted(set(int(x) for x in np.exp(rng.uniform(0, np.log(2 ** 22), 150)))) + [0, 1, 2 ** 22]
+        for eb, dtype in ((4, torch.float32), (2, torch.float16)):
+            t = base.view(dtype) if eb == 4 else base.view(torch.float16)
+            for n in sizes:
+                pieces = _page_dynamic_chunk_sized(t[:n], chunk_size)
+                k, c = orc.bucket_chunks_sized(n, eb, chunk_size)
+                assert k == len(pieces), (chunk_size, n, eb)
+                assert c == pieces[0].numel(), (chunk_size, n, eb)
+        off = orc.plan_chunks_ex(sizes, 4, orc.SCOPE_CHUNK, chunk_size)
+        pos = 0
+        for n in sizes:
+            k, c = orc.bucket_chunks_sized(n, 4, chunk_size)
+            assert off[pos + 1] - off[pos] == c or (n == 0 and c == 0)
+            pos += k
+        assert pos == len(off) - 1 and off[-1] == sum(sizes)
+
+
+def test_plan_default_chunk_size_is_the_page_plan(orc):
+    rng = np.random.default_rng(23)
+    buckets = [int(x) for x in rng.integers(0, 9_000_000, 20)] + [0, 1, 32768]
+    for eb in (2, 4):
+        assert np.array_equal(orc.plan_chunks_ex(buckets, eb, orc.SCOPE_CHUNK, 128 * 1024),
+                              orc.plan_chunks(buckets, eb))
+
+
+def test_plan_whole_bucket_and_whole_tensor_scopes(orc):
+    """One scale per bucket or per tensor: the table is the entries' boundaries, one chunk per
+    entry, an empty entry an empty chunk."""
+    sizes = [64, 0, 2359296, 1, 0, 513, 6553600, 3]
+    want = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    for scope in (orc.SCOPE_BUCKET, orc.SCOPE_TENSOR):
+        for eb in (2, 4):
+            assert np.array_equal(orc.plan_chunks_ex(sizes, eb, scope), want)
+
+
+def test_plan_ex_rejects_bad_arguments(orc):
+    import pytest
+    with pytest.raises(ValueError):
+        orc.plan_chunks_ex([10], 4, 3)
+    with pytest.raises(ValueError):
+        orc.plan_chunks_ex([10], 4, orc.SCOPE_CHUNK, 63)   # aligned part 0
+    with pytest.raises(ValueError):
+        orc.plan_chunks_ex([-1], 4, orc.SCOPE_TENSOR)
