@@ -48,6 +48,10 @@ def parse():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length (cpu_baseline)")
+    p.add_argument("--sweep", default=None, choices=["chunk", "order", "scope", "adaptive"],
+                   help="instead of the headline line: one JSON line per base chunk size (chunk), summation "
+                        "order (order) or scale scope (scope) of the pipelined kernel on the headline bucket, or "
+                        "the adaptive chunk-size chooser run online (adaptive)")
     p.add_argument("--entry", default="pipe", choices=["ws", "plain", "pipe"],
                    help="ws: gq_fused_allreduce_sim_ws (work-queue kernel); plain: gq_fused_allreduce_sim; "
                         "pipe: gq_fused_allreduce_sim_pipelined")
@@ -332,7 +336,7 @@ def run_gq(args):
         try:
             with open(tpath) as f:
                 tj = json.load(f).get(kernel, {})
-            if tj.get("kernel_source_hash") == kernel_source_hash():
+            if tj.get("kernel_source_hash") == kernel_source_hash(kernel):
                 traffic = tj.get("dram_bytes_per_launch")
         except (OSError, ValueError, AttributeError):
             traffic = None
@@ -368,23 +372,139 @@ def run_gq(args):
         dist.destroy_process_group()
 
 
-def kernel_source_hash():
-    """Hash of the device sources the timed kernels are built from (traffic figures taken from an
-    ncu capture count only while it matches)."""
+KERNEL_SOURCES = {
+    "k_pipe<f32>": ["gq_pipe.cuh", "gq_pipe_f32.cu", "gq_device.cuh", "gq_fused.cuh", "gq_internal.h"],
+    "k_queue<f32>": ["gq_queue.cuh", "gq_queue_f32.cu", "gq_device.cuh", "gq_fused.cuh", "gq_internal.h"],
+    "k_fused<f32, W=8>": ["gq_fused.cuh", "gq_fused_f32.cu", "gq_device.cuh", "gq_internal.h"],
+}
+
+
+def kernel_source_hash(kernel):
+    """Hash of the device sources the timed kernel is built from (a traffic figure taken from an
+    ncu capture counts only while it matches)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dp_gradient_bucket_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+SWEEP_CHUNKS = [16384, 32768, 65536, 131072, 262144, 524288, 1 << 20, 4 << 20]
+SWEEP_ORDERS = ["seq", "ring", "tree", "hier2", "hier4"]
+
+
+def run_sweep(args):
+    """Kernel time of the pipelined call on the headline bucket under other plans and orders.  Same
+    inputs, rotation over input sets larger than L2, and CUDA events on the launching stream as the
+    headline; the plan is made once per configuration (outside the timed launches)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import dp_gradient_bucket_gb300 as gq
+    import workloads as wl
+    from dp_gradient_bucket_gb300.chunker import DynamicChunker
+
+    host, stride = wl.rows(2, W, N_ELEMS)
+    base = torch.from_numpy(host).to(dev)
+    sets = [base.view(W, stride).roll(k, dims=0).reshape(-1).contiguous() for k in range(INPUT_SETS)]
+    del base
+    out = torch.empty(N_ELEMS, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    peak = float(measured_peaks()[0]["hbm_gbs"])
+    steps = max(20, min(args.steps, 400))
+    plans = {}
+
+    def plan(scope, chunk_bytes):
+        key = (scope, chunk_bytes)
+        if key not in plans:
+            nc = gq.gq_plan_chunks_ex([N_ELEMS], ELEM_BYTES, scope, chunk_bytes)
+            off = torch.empty(nc + 1, dtype=torch.int64, device=dev)
+            gq.gq_plan_chunks_ex([N_ELEMS], ELEM_BYTES, scope, chunk_bytes, off, stream)
+            ws = torch.zeros(gq.gq_pipelined_workspace_bytes(W, stride, nc), dtype=torch.uint8, device=dev)
+            plans[key] = (nc, off, ws)
+        return plans[key]
+
+    def launch(k, scope, chunk_bytes, order):
+        nc, off, ws = plan(scope, chunk_bytes)
+        gq.gq_fused_allreduce_sim_pipelined(sets[k % INPUT_SETS], W, stride, off, nc, 1.0, order, out, ws,
+                                            stream=stream)
+
+    def time_config(scope, chunk_bytes, order):
+        for k in range(max(args.warmup, 3)):
+            launch(k, scope, chunk_bytes, order)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for k in range(steps):
+            ev[k][0].record(stream)
+            launch(k, scope, chunk_bytes, order)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+        st = gq.gq_get_error(stream)
+        if st != gq.GQ_OK:
+            raise RuntimeError("device error: " + gq.gq_status_string(st))
+        us = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+        avg = sum(us) / len(us)
+        return {"chunks": plan(scope, chunk_bytes)[0], "kernel_avg_us": avg, "kernel_median_us": us[len(us) // 2],
+                "input_gbs": IN_BYTES / (avg * 1e-6) / 1e9,
+                "roofline_frac": (IN_BYTES + OUT_BYTES) / (avg * 1e-6) / 1e9 / peak}
+
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    w0 = time.time()
+    rows = []
+    if args.sweep == "chunk":
+        for cb in SWEEP_CHUNKS:
+            rows.append(dict({"sweep": "chunk_bytes", "chunk_bytes": cb, "order": "ring"}, **time_config("chunk", cb, "ring")))
+    elif args.sweep == "order":
+        for o in SWEEP_ORDERS:
+            rows.append(dict({"sweep": "order", "order": o, "chunk_bytes": 131072}, **time_config("chunk", 131072, o)))
+    elif args.sweep == "scope":
+        for sc in ("chunk", "bucket"):
+            rows.append(dict({"sweep": "scope", "scope": sc, "order": "ring"}, **time_config(sc, 131072, "ring")))
+    else:
+        # the chooser online: each step plans with its prediction and reports the step's kernel time,
+        # read one step late so that no step waits for its own events
+        ch = DynamicChunker(candidates=SWEEP_CHUNKS[1:7], explore_every=25)
+        for cb in ch.candidates:
+            for k in range(3):
+                launch(k, "chunk", cb, "ring")
+        torch.cuda.synchronize()
+        pending, picks = None, []
+        for k in range(steps):
+            cb = ch.predict_optimal()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch(k, "chunk", cb, "ring")
+            e1.record(stream)
+            if pending is not None:
+                pending[2].synchronize()
+                ch.update_metrics(pending[0], pending[1].elapsed_time(pending[2]) * 1e-3, IN_BYTES)
+            pending = (cb, e0, e1)
+            picks.append(cb)
+        torch.cuda.synchronize()
+        best = ch.best()
+        rows.append({"sweep": "adaptive", "steps": steps, "chosen_chunk_bytes": best,
+                     "picks_last_100": {str(c): picks[-100:].count(c) for c in ch.candidates},
+                     "ewma_us_per_step": {str(c): ch.ewma[c] * IN_BYTES * 1e6 for c in ch.candidates}})
+    w1 = time.time()
+    clocks.mark(w0, w1)
+    time.sleep(0.25)
+    clocks.stop()
+    summary = clocks.summary()
+    for r in rows:
+        r.update({"workload": WORKLOAD.replace(", ring order", ""), "peak_gbs": peak, "clocks": summary})
+        print(json.dumps(r), flush=True)
 
 
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
     else:
         run_gq(args)
 

@@ -4,7 +4,7 @@ Argument marshalling only.  Every step of the path runs in the library's CUDA ke
 PyTorch is used for device memory and streams.  There is no fallback: if libgq.so is
 missing or fails to load, importing the binding raises.
 
-Functions keep the C names: gq_plan_buckets, gq_plan_chunks, gq_quantize,
+Functions keep the C names: gq_plan_buckets, gq_plan_chunks, gq_plan_chunks_ex, gq_quantize,
 gq_reduce_dequant, gq_fused_allreduce_sim, gq_fused_workspace_bytes, gq_fused_allreduce_sim_ws,
 gq_pipelined_workspace_bytes, gq_fused_allreduce_sim_pipelined, gq_fused_allreduce_sim_static, gq_fused_allreduce_sim_amp, gq_amp_update_scale, gq_get_error,
 gq_status_string.  Device
@@ -66,6 +66,7 @@ def _load():
     sz, p, i32, i64 = ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
     L.gq_plan_buckets.argtypes = [p, sz, sz, sz, p, p, sz, p]
     L.gq_plan_chunks.argtypes = [p, sz, sz, p, sz, p, p]
+    L.gq_plan_chunks_ex.argtypes = [p, sz, sz, i32, sz, p, sz, p, p]
     L.gq_quantize.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, p, p, p]
     L.gq_reduce_dequant.argtypes = [p, p, i32, sz, p, sz, i32, p, p]
     L.gq_fused_allreduce_sim.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p]
@@ -84,7 +85,7 @@ def _load():
     L.gq_testing_inject_copy_stall.restype = i32
     L.gq_status_string.argtypes = [i32]
     L.gq_status_string.restype = ctypes.c_char_p
-    for name in ("gq_plan_buckets", "gq_plan_chunks", "gq_quantize", "gq_reduce_dequant",
+    for name in ("gq_plan_buckets", "gq_plan_chunks", "gq_plan_chunks_ex", "gq_quantize", "gq_reduce_dequant",
                  "gq_fused_allreduce_sim", "gq_fused_allreduce_sim_ws", "gq_fused_allreduce_sim_static",
                  "gq_fused_allreduce_sim_amp", "gq_fused_allreduce_sim_pipelined", "gq_amp_update_scale",
                  "gq_get_error"):
@@ -161,6 +162,27 @@ def gq_plan_chunks(bucket_elems, elem_bytes, d_offsets=None, stream=None):
                             0 if d_offsets is None else d_offsets.numel(), ctypes.byref(n),
                             _stream(stream) if d_offsets is not None else None)
     _check(st, "gq_plan_chunks")
+    return n.value
+
+
+GQ_SCOPE_CHUNK, GQ_SCOPE_BUCKET, GQ_SCOPE_TENSOR = 0, 1, 2
+SCOPES = {"chunk": GQ_SCOPE_CHUNK, "bucket": GQ_SCOPE_BUCKET, "tensor": GQ_SCOPE_TENSOR}
+GQ_CHUNK_SIZE = 128 * 1024
+
+
+def gq_plan_chunks_ex(elems, elem_bytes, scope="chunk", chunk_bytes=GQ_CHUNK_SIZE, d_offsets=None, stream=None):
+    """Chunk count of entries (buckets or tensors) laid end to end under a scale scope ("chunk",
+    "bucket", "tensor") and base chunk size; fills d_offsets on `stream` when given."""
+    be = np.ascontiguousarray(elems, dtype=np.uint64)
+    n = ctypes.c_size_t(0)
+    if d_offsets is not None:
+        import torch
+        if d_offsets.dtype != torch.int64:
+            raise TypeError("offsets must be int64")
+    st = lib.gq_plan_chunks_ex(be.ctypes.data, be.size, elem_bytes, SCOPES.get(scope, scope), chunk_bytes,
+                               _dptr(d_offsets), 0 if d_offsets is None else d_offsets.numel(), ctypes.byref(n),
+                               _stream(stream) if d_offsets is not None else None)
+    _check(st, "gq_plan_chunks_ex")
     return n.value
 
 

@@ -24,9 +24,9 @@ struct BucketPlan {
     uint64_t count;  // chunks
 };
 
-BucketPlan plan_one(uint64_t n, uint64_t eb) {
+BucketPlan plan_one(uint64_t n, uint64_t eb, uint64_t divisor = kDivisor) {
     if (n == 0) return {0, 1};  // torch.chunk of an empty tensor: one empty piece
-    uint64_t k = n * eb / kDivisor;
+    uint64_t k = n * eb / divisor;
     if (k < 1) k = 1;
     const uint64_t c = (n + k - 1) / k;
     return {c, (n + c - 1) / c};
@@ -116,38 +116,52 @@ gq_status gq_plan_buckets(const size_t* tensor_elems, size_t num_tensors, size_t
     return GQ_OK;
 }
 
-gq_status gq_plan_chunks(const size_t* bucket_elems, size_t num_buckets, size_t elem_bytes, int64_t* d_offsets,
-                         size_t offsets_capacity, size_t* num_chunks_out, gq_stream_t stream) {
-    if (!bucket_elems || !num_chunks_out || num_buckets == 0) return GQ_ERR_INVALID_ARG;
+gq_status gq_plan_chunks_ex(const size_t* elems, size_t count, size_t elem_bytes, gq_scope scope, size_t chunk_bytes,
+                            int64_t* d_offsets, size_t offsets_capacity, size_t* num_chunks_out, gq_stream_t stream) {
+    if (!elems || !num_chunks_out || count == 0) return GQ_ERR_INVALID_ARG;
     if (elem_bytes != 2 && elem_bytes != 4) return GQ_ERR_INVALID_ARG;
-    std::vector<gq::PlanBucket> plan(num_buckets);
+    if (scope != GQ_SCOPE_CHUNK && scope != GQ_SCOPE_BUCKET && scope != GQ_SCOPE_TENSOR) return GQ_ERR_INVALID_ARG;
+    // dynamic_chunk's divisor: the base size less its remainder modulo the 64-byte alignment
+    const uint64_t divisor = chunk_bytes - chunk_bytes % 64;
+    if (scope == GQ_SCOPE_CHUNK && (divisor == 0 || chunk_bytes > (static_cast<uint64_t>(1) << 40)))
+        return GQ_ERR_INVALID_ARG;
+    std::vector<gq::PlanBucket> plan(count);
     uint64_t total_chunks = 0, start = 0;
-    for (size_t b = 0; b < num_buckets; ++b) {
-        if (bucket_elems[b] > (static_cast<uint64_t>(1) << 40)) return GQ_ERR_INVALID_ARG;
-        const BucketPlan bp = plan_one(bucket_elems[b], elem_bytes);
+    for (size_t b = 0; b < count; ++b) {
+        if (elems[b] > (static_cast<uint64_t>(1) << 40)) return GQ_ERR_INVALID_ARG;
+        // whole-bucket / whole-tensor scope: the entry is one chunk (an empty one if n == 0)
+        const BucketPlan bp = scope == GQ_SCOPE_CHUNK ? plan_one(elems[b], elem_bytes, divisor)
+                                                      : BucketPlan{elems[b], 1};
         plan[b].elem_start = static_cast<int64_t>(start);
         plan[b].chunk_start = static_cast<int64_t>(total_chunks);
         plan[b].piece = static_cast<int64_t>(bp.piece);
         plan[b].count = static_cast<int64_t>(bp.count);
         total_chunks += bp.count;
-        start += bucket_elems[b];
+        start += elems[b];
     }
+    if (start > (static_cast<uint64_t>(1) << 40)) return GQ_ERR_INVALID_ARG;
     *num_chunks_out = static_cast<size_t>(total_chunks);
     if (!d_offsets) return GQ_OK;
     if (offsets_capacity < total_chunks + 1) return GQ_ERR_INVALID_ARG;
     if (!aligned(d_offsets, 8)) return GQ_ERR_MISALIGNED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    for (size_t b0 = 0; b0 < num_buckets; b0 += gq::kPlanBucketsPerLaunch) {
-        const size_t nb = num_buckets - b0 < static_cast<size_t>(gq::kPlanBucketsPerLaunch)
-                              ? num_buckets - b0
+    for (size_t b0 = 0; b0 < count; b0 += gq::kPlanBucketsPerLaunch) {
+        const size_t nb = count - b0 < static_cast<size_t>(gq::kPlanBucketsPerLaunch)
+                              ? count - b0
                               : static_cast<size_t>(gq::kPlanBucketsPerLaunch);
-        const bool last = b0 + nb == num_buckets;
+        const bool last = b0 + nb == count;
         const cudaError_t e = gq::launch_plan(plan.data() + b0, static_cast<int>(nb), d_offsets,
                                               last ? static_cast<int64_t>(total_chunks) : -1,
                                               static_cast<int64_t>(start), s);
         if (e != cudaSuccess) return from_cuda(e);
     }
     return GQ_OK;
+}
+
+gq_status gq_plan_chunks(const size_t* bucket_elems, size_t num_buckets, size_t elem_bytes, int64_t* d_offsets,
+                         size_t offsets_capacity, size_t* num_chunks_out, gq_stream_t stream) {
+    return gq_plan_chunks_ex(bucket_elems, num_buckets, elem_bytes, GQ_SCOPE_CHUNK, GQ_CHUNK_SIZE, d_offsets,
+                             offsets_capacity, num_chunks_out, stream);
 }
 
 // 0: not an order; 1: SEQ, RING or TREE; 2: hierarchical with a node size that divides W.

@@ -136,6 +136,31 @@ gq_status gq_plan_chunks(const size_t* bucket_elems, size_t num_buckets, size_t 
                          int64_t* d_offsets, size_t offsets_capacity, size_t* num_chunks_out,
                          gq_stream_t stream);
 
+/* Base chunk size of dynamic_chunk (the article's CHUNK_SIZE knob, §4.2; 128 KiB). */
+#define GQ_CHUNK_SIZE ((size_t)128 * 1024)
+
+/* What one quantisation scale (and one allreduce unit, hence one set of ring segments) covers.
+ *   GQ_SCOPE_CHUNK   dynamic_chunk pieces of every entry; the entries are buckets.
+ *   GQ_SCOPE_BUCKET  each entry (a bucket) is one chunk: one scale per bucket.
+ *   GQ_SCOPE_TENSOR  each entry (a tensor) is one chunk: one scale per tensor.
+ * The article's quantize_gradient takes "the gradient" it is handed whole (§2.2.1) without
+ * saying whether that is a chunk, a bucket or a tensor; the per-chunk scope follows its per-chunk
+ * allreduce (§3.1) and is the default, the other two are the whole-gradient readings. */
+typedef enum { GQ_SCOPE_CHUNK = 0, GQ_SCOPE_BUCKET = 1, GQ_SCOPE_TENSOR = 2 } gq_scope;
+
+/* gq_plan_chunks generalised: entries (buckets, or tensors) laid end to end, cut under `scope`.
+ *   elems[count]  host array of entry sizes in elements (count >= 1); an empty entry is one empty
+ *                 chunk under every scope
+ *   chunk_bytes   GQ_SCOPE_CHUNK only: the base chunk size, so that a bucket of n elements gets
+ *                 k = max(1, n*elem_bytes // (chunk_bytes - chunk_bytes % 64)) requested pieces
+ *                 (GQ_ERR_INVALID_ARG if that divisor is 0); ignored by the other scopes
+ *   the rest      as gq_plan_chunks, which is gq_plan_chunks_ex(..., GQ_SCOPE_CHUNK, GQ_CHUNK_SIZE, ...).
+ * The quantise and reduce calls take the table whatever the scope; chunks longer than the
+ * pipelined kernel's shared-memory ring (176 KiB of input per rank) are read twice. */
+gq_status gq_plan_chunks_ex(const size_t* elems, size_t count, size_t elem_bytes, gq_scope scope,
+                            size_t chunk_bytes, int64_t* d_offsets, size_t offsets_capacity,
+                            size_t* num_chunks_out, gq_stream_t stream);
+
 /* quantize_gradient per (rank, chunk) (pipelined-AllReduce article §2.2.1), after the
  * optional unscale of §6.1:
  *   g = float(x) * inv, inv = (float)(1.0 / (double)loss_scale)    (loss_scale 1: g = x)

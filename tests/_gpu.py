@@ -30,21 +30,28 @@ def guards_intact(buf, n):
     return bool((head == want).all()) and bool((tail == want).all())
 
 
-def plan_device(bucket_elems, eb, dev, stream=None):
-    nc = gq.gq_plan_chunks(bucket_elems, eb)
+def plan_device(bucket_elems, eb, dev, stream=None, scope=None, chunk_bytes=None):
+    if scope is None and chunk_bytes is None:
+        nc = gq.gq_plan_chunks(bucket_elems, eb)
+        offsets = torch.full((nc + 1,), -1, dtype=torch.int64, device=dev)
+        gq.gq_plan_chunks(bucket_elems, eb, offsets, stream=stream)
+        return nc, offsets
+    scope = scope or "chunk"
+    chunk_bytes = chunk_bytes or gq.GQ_CHUNK_SIZE
+    nc = gq.gq_plan_chunks_ex(bucket_elems, eb, scope, chunk_bytes)
     offsets = torch.full((nc + 1,), -1, dtype=torch.int64, device=dev)
-    gq.gq_plan_chunks(bucket_elems, eb, offsets, stream=stream)
+    gq.gq_plan_chunks_ex(bucket_elems, eb, scope, chunk_bytes, offsets, stream=stream)
     return nc, offsets
 
 
 def run(host_rows, W, stride, bucket_elems, order, loss_scale=1.0, mode="fused", dev="cuda:0",
-        offsets=None, want_codes=True):
+        offsets=None, want_codes=True, scope=None, chunk_bytes=None):
     """Runs the path on the GPU.  Returns (out, codes, scales, offsets_host, status) as numpy."""
     dev = torch.device(dev)
     eb = host_rows.dtype.itemsize
     grads = torch.from_numpy(host_rows).to(dev)
     if offsets is None:
-        nc, d_off = plan_device(bucket_elems, eb, dev)
+        nc, d_off = plan_device(bucket_elems, eb, dev, scope=scope, chunk_bytes=chunk_bytes)
     else:
         d_off = torch.from_numpy(np.ascontiguousarray(offsets, dtype=np.int64)).to(dev)
         nc = len(offsets) - 1

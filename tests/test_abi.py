@@ -68,6 +68,25 @@ def test_plan_chunk_count_matches_oracle(gq, orc):
         assert gq.gq_plan_chunks(buckets, eb) == len(orc.plan_chunks(buckets, eb)) - 1
 
 
+def test_plan_chunks_ex_count_matches_oracle(gq, orc):
+    """Chunk counts (host-side, no device table) for other base chunk sizes and the whole-bucket
+    and whole-tensor scopes."""
+    rng = np.random.default_rng(4)
+    sizes = [int(x) for x in rng.integers(0, 3_000_000, 30)] + [0, 1, 65536]
+    for eb in (2, 4):
+        for cb in (100, 16384, 32868, 262144, 1 << 20):
+            assert gq.gq_plan_chunks_ex(sizes, eb, "chunk", cb) == \
+                len(orc.plan_chunks_ex(sizes, eb, orc.SCOPE_CHUNK, cb)) - 1
+        for scope in ("bucket", "tensor"):
+            assert gq.gq_plan_chunks_ex(sizes, eb, scope) == len(sizes)
+    L = gq.lib
+    n = ctypes.c_size_t(0)
+    be = (ctypes.c_size_t * 2)(100, 200)
+    assert L.gq_plan_chunks_ex(be, 2, 4, 0, 63, None, 0, ctypes.byref(n), None) == gq.GQ_ERR_INVALID_ARG
+    assert L.gq_plan_chunks_ex(be, 2, 4, 3, 131072, None, 0, ctypes.byref(n), None) == gq.GQ_ERR_INVALID_ARG
+    assert L.gq_plan_chunks_ex(be, 2, 4, 2, 0, None, 0, ctypes.byref(n), None) == gq.GQ_OK and n.value == 2
+
+
 def _call_fused(gq, grads=0x10000, dt=0, W=8, stride=1024, offsets=0x20000, nc=4, ls=1.0, order=1,
                 out=0x30000, codes=None, scales=None):
     return gq.lib.gq_fused_allreduce_sim(grads, dt, W, stride, offsets, nc, ls, order, out, codes, scales, None)
