@@ -48,7 +48,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=50)
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length (cpu_baseline)")
-    p.add_argument("--sweep", default=None, choices=["chunk", "order", "scope", "adaptive"],
+    p.add_argument("--bwd-k", type=int, default=512, help="inner size of the synthetic backward GEMM (--sweep overlap)")
+    p.add_argument("--sweep", default=None, choices=["chunk", "order", "scope", "adaptive", "overlap"],
                    help="instead of the headline line: one JSON line per base chunk size (chunk), summation "
                         "order (order) or scale scope (scope) of the pipelined kernel on the headline bucket, or "
                         "the adaptive chunk-size chooser run online (adaptive)")
@@ -499,10 +500,121 @@ def run_sweep(args):
         print(json.dumps(r), flush=True)
 
 
+def run_overlap(args):
+    """Backward / allreduce overlap, the pages' PipelineController with PIPELINE_DEPTH = 2: a
+    synthetic backward pass writes the gradients of B buckets (W = 8 rank rows of 2560 x 2560 fp32,
+    one TF32 batched GEMM each, on a compute stream) into two alternating buffers; each bucket's
+    pipelined int8 allreduce runs on a high-priority stream once its gradients exist, and the
+    backward of bucket b + 2 waits until the allreduce of bucket b has read its buffer.  Times (CUDA
+    events, averaged over repetitions): backward alone, allreduce alone, both one after the other on
+    one stream, and the two-stream pipeline for several caps on the allreduce's SMs."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import dp_gradient_bucket_gb300 as gq
+    torch.backends.cuda.matmul.allow_tf32 = True
+    B, side, K = 8, 2560, args.bwd_k
+    n = side * side  # 6,553,600: the 25 MiB bucket
+    g = torch.Generator(device=dev)
+    g.manual_seed(0x6751)
+    A = torch.randn(W, side, K, device=dev, generator=g) * 1e-2
+    Bm = torch.randn(W, K, side, device=dev, generator=g) * 1e-2
+    grads = [torch.empty(W, side, side, device=dev) for _ in range(2)]
+    outs = [torch.empty(n, device=dev) for _ in range(B)]
+    nc = gq.gq_plan_chunks([n], 4)
+    off = torch.empty(nc + 1, dtype=torch.int64, device=dev)
+    main = torch.cuda.current_stream(dev)
+    gq.gq_plan_chunks([n], 4, off, main)
+    ws = torch.zeros(gq.gq_pipelined_workspace_bytes(W, n, nc), dtype=torch.uint8, device=dev)
+    s_bwd = torch.cuda.Stream(dev)
+    s_comm = torch.cuda.Stream(dev, priority=-1)
+    reps = max(3, min(args.steps, 30))
+
+    def bwd(b, stream):
+        with torch.cuda.stream(stream):
+            torch.bmm(A, Bm, out=grads[b % 2])
+
+    def comm(b, stream, max_ctas):
+        gq.gq_fused_allreduce_sim_pipelined(grads[b % 2].view(-1), W, n, off, nc, 1.0, "ring", outs[b], ws,
+                                            stream=stream, max_ctas=max_ctas)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        for _ in range(reps):
+            fn()
+        e1.record(main)
+        torch.cuda.synchronize()
+        st = gq.gq_get_error(main)
+        if st != gq.GQ_OK:
+            raise RuntimeError("device error: " + gq.gq_status_string(st))
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    def only_bwd():
+        for b in range(B):
+            bwd(b, main)
+
+    def only_comm():
+        for b in range(B):
+            comm(b, main, 0)
+
+    def only_comm_capped(cap):
+        for b in range(B):
+            comm(b, main, cap)
+
+    def serial(max_ctas=0):
+        for b in range(B):
+            bwd(b, main)
+            comm(b, main, max_ctas)
+
+    def pipelined(max_ctas):
+        done_bwd = [torch.cuda.Event() for _ in range(B)]
+        done_comm = [torch.cuda.Event() for _ in range(B)]
+        start = torch.cuda.Event()
+        start.record(main)
+        s_bwd.wait_event(start)
+        s_comm.wait_event(start)
+        for b in range(B):
+            if b >= 2:
+                s_bwd.wait_event(done_comm[b - 2])  # the buffer is free again
+            bwd(b, s_bwd)
+            done_bwd[b].record(s_bwd)
+            s_comm.wait_event(done_bwd[b])
+            comm(b, s_comm, max_ctas)
+            done_comm[b].record(s_comm)
+        main.wait_event(done_comm[B - 1])
+        main.wait_event(done_bwd[B - 1])
+
+    t_bwd = timed(only_bwd)
+    t_comm = timed(only_comm)
+    t_serial = timed(serial)
+    serial()
+    torch.cuda.synchronize()
+    ref = [o.clone() for o in outs]
+    rows = []
+    for cap in (0, 128, 96, 64, 32, 16):
+        t_c = timed(lambda: only_comm_capped(cap)) if cap else t_comm
+        t_pipe = timed(lambda: pipelined(cap))
+        same = all(torch.equal(o.view(torch.int32), r.view(torch.int32)) for o, r in zip(outs, ref))
+        rows.append({"sweep": "overlap", "max_ctas": cap or "all", "buckets": B, "bwd_gemm": "TF32 bmm [8,2560,%d]x[8,%d,2560]" % (K, K),
+                     "t_bwd_us": t_bwd, "t_comm_us": t_c, "t_serial_us": t_serial, "t_pipelined_us": t_pipe,
+                     "hidden_frac_of_shorter": (t_bwd + t_c - t_pipe) / min(t_bwd, t_c),
+                     "speedup_vs_serial": t_serial / t_pipe, "ideal_us": max(t_bwd, t_c),
+                     "outputs_equal_serial": bool(same)})
+
+    for r in rows:
+        print(json.dumps(r), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep == "overlap":
+        run_overlap(args)
     elif args.sweep:
         run_sweep(args)
     else:

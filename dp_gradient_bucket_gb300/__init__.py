@@ -6,7 +6,7 @@ missing or fails to load, importing the binding raises.
 
 Functions keep the C names: gq_plan_buckets, gq_plan_chunks, gq_plan_chunks_ex, gq_quantize,
 gq_reduce_dequant, gq_fused_allreduce_sim, gq_fused_workspace_bytes, gq_fused_allreduce_sim_ws,
-gq_pipelined_workspace_bytes, gq_fused_allreduce_sim_pipelined, gq_fused_allreduce_sim_static, gq_fused_allreduce_sim_amp, gq_amp_update_scale, gq_get_error,
+gq_pipelined_workspace_bytes, gq_fused_allreduce_sim_pipelined(_ex), gq_fused_allreduce_sim_static, gq_fused_allreduce_sim_amp, gq_amp_update_scale, gq_get_error,
 gq_status_string.  Device
 arguments are CUDA torch tensors (contiguous; their storage is used as is); `stream` is a
 torch.cuda.Stream, a raw cudaStream_t integer, or None for torch's current stream.
@@ -76,6 +76,8 @@ def _load():
     L.gq_amp_update_scale.argtypes = [p, p, p, ctypes.c_float, ctypes.c_float, i32, p]
     L.gq_fused_allreduce_sim_pipelined.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p, p, sz,
                                                    p]
+    L.gq_fused_allreduce_sim_pipelined_ex.argtypes = [p, i32, i32, sz, p, sz, ctypes.c_float, i32, p, p, p, p, p,
+                                                      sz, i32, p]
     L.gq_pipelined_workspace_bytes.argtypes = [i32, sz, sz]
     L.gq_pipelined_workspace_bytes.restype = sz
     L.gq_fused_workspace_bytes.argtypes = [sz, i32]
@@ -87,7 +89,8 @@ def _load():
     L.gq_status_string.restype = ctypes.c_char_p
     for name in ("gq_plan_buckets", "gq_plan_chunks", "gq_plan_chunks_ex", "gq_quantize", "gq_reduce_dequant",
                  "gq_fused_allreduce_sim", "gq_fused_allreduce_sim_ws", "gq_fused_allreduce_sim_static",
-                 "gq_fused_allreduce_sim_amp", "gq_fused_allreduce_sim_pipelined", "gq_amp_update_scale",
+                 "gq_fused_allreduce_sim_amp", "gq_fused_allreduce_sim_pipelined",
+                 "gq_fused_allreduce_sim_pipelined_ex", "gq_amp_update_scale",
                  "gq_get_error"):
         getattr(L, name).restype = i32
     return L
@@ -227,16 +230,25 @@ def gq_pipelined_workspace_bytes(W, rank_stride, num_chunks):
 
 
 def gq_fused_allreduce_sim_pipelined(grads, W, rank_stride, d_offsets, num_chunks, loss_scale, order, out, workspace,
-                                     codes=None, scales=None, found_inf=None, stream=None):
+                                     codes=None, scales=None, found_inf=None, stream=None, max_ctas=None):
     """gq_fused_allreduce_sim as the quantise / reduce pipeline through L2.  `workspace` is a CUDA
     tensor of at least gq_pipelined_workspace_bytes(W, rank_stride, num_chunks) bytes, 256-byte
     aligned, zero-filled before its first use and then passed unchanged from call to call (zero it
-    again only after a GQ_ERR_TIMEOUT); `found_inf` (optional) a one-element float32 CUDA tensor."""
-    st = lib.gq_fused_allreduce_sim_pipelined(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
-                                              num_chunks, loss_scale, _order(order), _dptr(out),
-                                              _dptr(codes), _dptr(scales), _dptr(found_inf), _dptr(workspace),
-                                              workspace.numel() * workspace.element_size(), _stream(stream))
-    _check(st, "gq_fused_allreduce_sim_pipelined")
+    again only after a GQ_ERR_TIMEOUT); `found_inf` (optional) a one-element float32 CUDA tensor.
+    `max_ctas` (optional) caps the SMs it runs on (gq_fused_allreduce_sim_pipelined_ex)."""
+    if max_ctas is None:
+        st = lib.gq_fused_allreduce_sim_pipelined(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
+                                                  num_chunks, loss_scale, _order(order), _dptr(out),
+                                                  _dptr(codes), _dptr(scales), _dptr(found_inf), _dptr(workspace),
+                                                  workspace.numel() * workspace.element_size(), _stream(stream))
+        _check(st, "gq_fused_allreduce_sim_pipelined")
+        return
+    st = lib.gq_fused_allreduce_sim_pipelined_ex(_dptr(grads), _dtype_code(grads), W, rank_stride, _dptr(d_offsets),
+                                                 num_chunks, loss_scale, _order(order), _dptr(out),
+                                                 _dptr(codes), _dptr(scales), _dptr(found_inf), _dptr(workspace),
+                                                 workspace.numel() * workspace.element_size(), int(max_ctas),
+                                                 _stream(stream))
+    _check(st, "gq_fused_allreduce_sim_pipelined_ex")
 
 
 def gq_fused_allreduce_sim_static(grads, W, rank_stride, d_offsets, num_chunks, loss_scale, order, out, codes=None,

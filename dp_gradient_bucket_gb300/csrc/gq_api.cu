@@ -309,9 +309,19 @@ gq_status gq_fused_allreduce_sim_pipelined(const void* d_grads, gq_dtype dt, int
                                            gq_order order, float* d_out, int8_t* d_codes_opt, float* d_scales_opt,
                                            float* d_found_inf_opt, void* d_workspace, size_t workspace_bytes,
                                            gq_stream_t stream) {
+    return gq_fused_allreduce_sim_pipelined_ex(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale, order,
+                                               d_out, d_codes_opt, d_scales_opt, d_found_inf_opt, d_workspace,
+                                               workspace_bytes, 0, stream);
+}
+
+gq_status gq_fused_allreduce_sim_pipelined_ex(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                              const int64_t* d_offsets, size_t num_chunks, float loss_scale,
+                                              gq_order order, float* d_out, int8_t* d_codes_opt,
+                                              float* d_scales_opt, float* d_found_inf_opt, void* d_workspace,
+                                              size_t workspace_bytes, int max_ctas, gq_stream_t stream) {
     gq_status st = check_grads(d_grads, dt, W, rank_stride, d_offsets, num_chunks, loss_scale);
     if (st != GQ_OK) return st;
-    if (!d_out || !d_workspace) return GQ_ERR_INVALID_ARG;
+    if (!d_out || !d_workspace || max_ctas < 0) return GQ_ERR_INVALID_ARG;
     if (!order_kind(order, W)) return GQ_ERR_INVALID_ARG;
     if (workspace_bytes < gq_pipelined_workspace_bytes(W, rank_stride, num_chunks)) return GQ_ERR_INVALID_ARG;
     if (!aligned(d_out, 16) || !aligned(d_workspace, 256) || (d_codes_opt && !aligned(d_codes_opt, 16)) ||
@@ -330,9 +340,9 @@ gq_status gq_fused_allreduce_sim_pipelined(const void* d_grads, gq_dtype dt, int
     a.found_inf = d_found_inf_opt;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return from_cuda(dt == GQ_F32 ? gq::launch_pipe_f32(a, static_cast<int>(order), d_out, d_codes_opt, d_scales_opt,
-                                                        d_workspace, s)
+                                                        d_workspace, max_ctas, s)
                                   : gq::launch_pipe_f16(a, static_cast<int>(order), d_out, d_codes_opt, d_scales_opt,
-                                                        d_workspace, s));
+                                                        d_workspace, max_ctas, s));
 }
 
 }  // extern "C"

@@ -87,10 +87,11 @@ cudaError_t queue_f16_set_stall(uint32_t extra_bytes, uint64_t limit_ns);
 // pipe_workspace_bytes(W, rank_stride, num_chunks) bytes, 256-byte aligned, zero-filled before its
 // first launch.
 size_t pipe_workspace_bytes(int W, int64_t rank_stride, int64_t num_chunks);
+// max_ctas > 0 caps the persistent grid (the other SMs stay free for concurrent kernels).
 cudaError_t launch_pipe_f32(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales, void* workspace,
-                            cudaStream_t stream);
+                            int max_ctas, cudaStream_t stream);
 cudaError_t launch_pipe_f16(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales, void* workspace,
-                            cudaStream_t stream);
+                            int max_ctas, cudaStream_t stream);
 cudaError_t pipe_f32_read_clear_error(unsigned* word);
 cudaError_t pipe_f16_read_clear_error(unsigned* word);
 cudaError_t pipe_f32_set_stall(uint32_t extra_bytes, uint64_t limit_ns);

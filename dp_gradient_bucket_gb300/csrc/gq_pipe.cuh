@@ -1092,7 +1092,7 @@ inline void init_pipe(PipeInit* pi) {
 // 256-byte aligned, zero-filled before its first launch.
 template <int DT>
 inline cudaError_t launch_pipe_dt(PipeInit* table, const QuantArgs& a, int order, float* out, int8_t* codes,
-                                  float* scales, void* ws, cudaStream_t stream) {
+                                  float* scales, void* ws, int max_ctas, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1119,8 +1119,12 @@ inline cudaError_t launch_pipe_dt(PipeInit* table, const QuantArgs& a, int order
     P.cstride = code_stride(a.rank_stride);
     P.total_q = static_cast<unsigned long long>(a.num_chunks) * static_cast<unsigned long long>(a.W);
     P.total_r = static_cast<unsigned long long>(a.num_chunks) * static_cast<unsigned long long>(P.nseg);
-    const unsigned long long want = P.total_q;
-    const unsigned grid = static_cast<unsigned>(want < static_cast<unsigned long long>(pi.ctas) ? want : pi.ctas);
+    // any grid works (items are claimed from counters): at most one CTA per SM, per quantise item,
+    // and per the caller's cap
+    unsigned long long want = P.total_q;
+    if (want > static_cast<unsigned long long>(pi.ctas)) want = static_cast<unsigned long long>(pi.ctas);
+    if (max_ctas > 0 && want > static_cast<unsigned long long>(max_ctas)) want = static_cast<unsigned long long>(max_ctas);
+    const unsigned grid = static_cast<unsigned>(want);
     if (P.hier_L > 0)
         k_pipe<DT, true><<<grid, kThreads, kSmemBytes, stream>>>(P);
     else

@@ -6,8 +6,8 @@ namespace gq {
 static pipe::PipeInit g_pipe_init_f16[64];
 
 cudaError_t launch_pipe_f16(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales, void* workspace,
-                            cudaStream_t stream) {
-    return pipe::launch_pipe_dt<1>(g_pipe_init_f16, a, order, out, codes, scales, workspace, stream);
+                            int max_ctas, cudaStream_t stream) {
+    return pipe::launch_pipe_dt<1>(g_pipe_init_f16, a, order, out, codes, scales, workspace, max_ctas, stream);
 }
 
 cudaError_t pipe_f16_read_clear_error(unsigned* word) { return fused::read_clear_error(word); }

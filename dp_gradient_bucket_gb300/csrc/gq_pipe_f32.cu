@@ -10,8 +10,8 @@ size_t pipe_workspace_bytes(int W, int64_t rank_stride, int64_t num_chunks) {
 }
 
 cudaError_t launch_pipe_f32(const QuantArgs& a, int order, float* out, int8_t* codes, float* scales, void* workspace,
-                            cudaStream_t stream) {
-    return pipe::launch_pipe_dt<0>(g_pipe_init_f32, a, order, out, codes, scales, workspace, stream);
+                            int max_ctas, cudaStream_t stream) {
+    return pipe::launch_pipe_dt<0>(g_pipe_init_f32, a, order, out, codes, scales, workspace, max_ctas, stream);
 }
 
 cudaError_t pipe_f32_read_clear_error(unsigned* word) { return fused::read_clear_error(word); }

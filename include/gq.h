@@ -271,6 +271,17 @@ gq_status gq_fused_allreduce_sim_pipelined(const void* d_grads, gq_dtype dt, int
                                            float* d_found_inf_opt, void* d_workspace, size_t workspace_bytes,
                                            gq_stream_t stream);
 
+/* gq_fused_allreduce_sim_pipelined on at most max_ctas SMs (max_ctas > 0; 0: one CTA on every SM, as
+ * gq_fused_allreduce_sim_pipelined).  The article's pipeline (§2.1, §3.1 PipelineController) runs the
+ * allreduce of one bucket while the backward pass computes the next: a cap leaves the other SMs to
+ * kernels on other streams.  Same results, bit for bit, for any cap (work is claimed from counters,
+ * and no wait depends on a CTA that has not started).  GQ_ERR_INVALID_ARG if max_ctas < 0. */
+gq_status gq_fused_allreduce_sim_pipelined_ex(const void* d_grads, gq_dtype dt, int W, size_t rank_stride,
+                                              const int64_t* d_offsets, size_t num_chunks, float loss_scale,
+                                              gq_order order, float* d_out, int8_t* d_codes_opt,
+                                              float* d_scales_opt, float* d_found_inf_opt, void* d_workspace,
+                                              size_t workspace_bytes, int max_ctas, gq_stream_t stream);
+
 /* Bytes of the library's own device scratch array used by gq_fused_allreduce_sim_static: 1 MiB,
  * enough for chunk tables of up to 511 chunks at W = 8 (buckets of up to 64 MiB of fp32, or
  * 128 MiB of fp16, per rank under dynamic_chunk). */

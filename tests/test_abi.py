@@ -186,6 +186,9 @@ def test_pipelined_rejects_bad_arguments(gq):
     assert _call_pipe(gq, order=3) == BAD
     assert _call_pipe(gq, order=0x100) == BAD
     assert _call_pipe(gq, order=0x100 + 5) == BAD   # L = 5 does not divide W = 8
+    need = gq.gq_pipelined_workspace_bytes(8, 1024, 4)
+    assert gq.lib.gq_fused_allreduce_sim_pipelined_ex(0x10000, 0, 8, 1024, 0x20000, 4, 1.0, 1, 0x30000, None, None,
+                                                      None, 0x100000, need, -1, None) == BAD
     assert _call_pipe(gq, ls=0.0) == BAD
     need = gq.gq_pipelined_workspace_bytes(8, 1024, 4)
     assert _call_pipe(gq, ws_bytes=need - 1) == BAD

@@ -68,6 +68,25 @@ def test_pipe_many_items_per_cta_with_two_pass_chunks(W, dt):
             H.assert_bits_equal(out, want, "output of call %d" % rep)
 
 
+@pytest.mark.parametrize("max_ctas", [1, 7, 40, 100000])
+def test_pipe_capped_grid(max_ctas):
+    """The capped grid (gq_fused_allreduce_sim_pipelined_ex) gives the same bits for any cap, down to
+    one CTA doing every item of both stages."""
+    W, n = 8, 300007
+    host, stride = wl.rows(2, W, n)
+    dev = torch.device("cuda:0")
+    grads = torch.from_numpy(host).to(dev)
+    nc, d_off = H.plan_device([n], 4, dev)
+    out = torch.zeros(n, dtype=torch.float32, device=dev)
+    ws = _ws(W, stride, nc, dev)
+    want = oracle.fused(host, W, stride, d_off.cpu().numpy(), oracle.RING)[0]
+    for _ in range(2):
+        gq.gq_fused_allreduce_sim_pipelined(grads, W, stride, d_off, nc, 1.0, "ring", out, ws, max_ctas=max_ctas)
+        assert gq.gq_get_error() == gq.GQ_OK
+        H.assert_bits_equal(out.cpu().numpy(), want, "output")
+    assert H.pipe_header(ws) == (0, 0, 0, 2)
+
+
 @pytest.mark.parametrize("W", [8, 16])
 def test_pipe_fp16_unscale(W):
     """fp16 gradients with loss scales 65536 (exact unscale) and 3 (inexact), every order."""
