@@ -65,7 +65,14 @@ constexpr int kQBar = 1;   // named barrier of the quantisers (0 is __syncthread
 #define GQ_PIPE_RBUF_CODES 16384
 #endif
 constexpr int kRBufCodes = GQ_PIPE_RBUF_CODES;
-constexpr int kRSlack = 32;
+// A unit of E elements (E a multiple of 128) starting anywhere is copied from its 16-byte-aligned
+// start to its 16-byte-aligned end: at most E + 16 bytes per row.
+#ifndef GQ_PIPE_RSLACK
+#define GQ_PIPE_RSLACK 16
+#endif
+constexpr int kRSlack = GQ_PIPE_RSLACK;
+static_assert(kRSlack >= 16 && kRSlack % 16 == 0, "row slack");
+static_assert(kRBufCodes / kMaxRanks >= 128, "a reduce unit must hold at least 128 elements at W = 64");
 constexpr int kRBufBytes = kRBufCodes + kMaxRanks * kRSlack;
 constexpr size_t kSmemBytes = static_cast<size_t>(kSlots) * kPiece + 2 * kRBufBytes;
 static_assert(kInfo > kSlots, "an item descriptor must outlive the pieces issued after it");
@@ -115,7 +122,7 @@ inline size_t workspace_bytes(int W, int64_t rank_stride, int64_t num_chunks) {
 struct PArgs {
     QuantArgs q;
     int order;
-    int hier_L;  // hierarchical order: ranks per node (0 under the other orders)
+    int hier_L;  // tree-like orders: ranks per node (the hierarchical order's L; 1 for the tree order; else 0)
     int nseg;    // reduce items per chunk: the segments of torch.chunk(chunk, nseg) (L, else W)
     float* out;
     int8_t* codes_out;  // [W][rank_stride], may be null
@@ -727,7 +734,7 @@ static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf,
         }
         fence_acq_rel_gpu();         // acquire: the codes stored before the words
         fence_proxy_async_global();  // ... and before the bulk copies that read them
-        const int rot = ring ? (t + 1 == W ? 0 : t + 1) : L > 0 ? (t + 1 == L ? 0 : t + 1) : 0;
+        const int rot = ring ? (t + 1 == W ? 0 : t + 1) : L > 0 ? (t + 1) % L : 0;
         for (int64_t x = a; x < b; x += E) {
             if (!acquire(useq)) {
                 ok = false;
@@ -835,34 +842,6 @@ __device__ __forceinline__ void reduce_group16(const PArgs& P, const unsigned ch
     }
 }
 
-// The same under the tree order, two elements at a time (ranks in index order).
-__device__ __forceinline__ void reduce_group16_tree(const PArgs& P, const unsigned char* base, uint32_t row,
-                                                   const float* sc, int W, int64_t e0, int64_t c0, int64_t a,
-                                                   int64_t b, bool pow2) {
-#pragma unroll 1
-    for (int q = 0; q < 8; ++q) {
-        const int64_t f0 = e0 + 2 * q;
-        if (f0 + 2 <= a || f0 >= b) continue;
-        const uint32_t off = static_cast<uint32_t>(f0 - c0);
-        TreeAcc tr[2];
-        tr[0].init();
-        tr[1].init();
-        for (int r = 0; r < W; ++r) {
-            const uint32_t wx = (ld_shared_u32(base + r * row + (off & ~3u)) >> (8 * (off & 3u))) ^ 0x8080u;
-            const float s = sc[r];
-            tr[0].push(__fmul_rn(__fsub_rn(code_biased(wx, 0), kCodeBias), s));
-            tr[1].push(__fmul_rn(__fsub_rn(code_biased(wx, 1), kCodeBias), s));
-        }
-        const float o0 = mean_of(tr[0].result(), W, P.invW, pow2), o1 = mean_of(tr[1].result(), W, P.invW, pow2);
-        if (f0 >= a && f0 + 2 <= b) {
-            *reinterpret_cast<float2*>(P.out + f0) = make_float2(o0, o1);
-        } else {
-            if (f0 >= a && f0 < b) P.out[f0] = o0;
-            if (f0 + 1 >= a && f0 + 1 < b) P.out[f0 + 1] = o1;
-        }
-    }
-}
-
 // TreeAcc on packed pairs: pairwise sums in push order, an odd one carried up a level, for up
 // to 127 pushes (a binary counter of partial sums; st[b] holds a sum of 2^b pushes).
 struct TreeAcc2 {
@@ -899,55 +878,114 @@ struct TreeAcc2 {
     }
 };
 
-// The same under the hierarchical order, two elements (one packed pair) at a time: per node of
-// L consecutive ranks, the node's ranks in ring order from local rank `rot`, then the node sums
-// by the tree rule.
-__device__ __forceinline__ void reduce_group16_hier(const PArgs& P, const unsigned char* base, uint32_t row,
-                                                   const float* sc, int W, int L, int rot, int64_t e0, int64_t c0,
-                                                   int64_t a, int64_t b, bool pow2) {
+// The hierarchical order (and, with L = 1, the tree order) on the 4 elements [4w, 4w + 4) of a reduce
+// unit: per node of L consecutive ranks, the node's ranks in ring order from local rank `rot`, then
+// the node sums by the tree rule, two packed pairs at a time.  Consecutive lanes take consecutive
+// words, so the 4-byte shared-memory loads of a warp are conflict-free and its float4 stores
+// coalesced.  NODES > 0: the node count W / L as a compile-time constant, so the tree's binary
+// counter folds away (no branches, only the NODES - 1 additions); NODES = 0: any count, at run time.
+// LC > 0: the node size L as a compile-time constant (the node's ring unrolled); LC = 1 is the tree
+// order, each node sum one dequantised rank.
+template <int NODES, int LC>
+__device__ __forceinline__ void reduce_word4_hier(const PArgs& P, const unsigned char* base, uint32_t row,
+                                                 const float* sc, int W, int L, int rot, int64_t w, int64_t c0,
+                                                 int64_t a, int64_t b, bool pow2) {
     const uint64_t C2 = pk(kCodeBias, kCodeBias);
     const uint64_t z2 = pk(P.neg_zero, P.neg_zero);
-#pragma unroll 1
-    for (int q = 0; q < 8; ++q) {
-        const int64_t f0 = e0 + 2 * q;
-        if (f0 + 2 <= a || f0 >= b) continue;
-        const uint32_t off = static_cast<uint32_t>(f0 - c0);
-        TreeAcc2 tr;
-        tr.init();
-        for (int nb = 0; nb < W; nb += L) {
-            uint64_t n0 = 0;
-            int r = rot;
-            for (int k = 0; k < L; ++k) {
-                const uint32_t wx = (ld_shared_u32(base + (nb + r) * row + (off & ~3u)) >> (8 * (off & 3u))) ^ 0x8080u;
+    const int64_t f0 = 4 * w;
+    const uint32_t off = static_cast<uint32_t>(f0 - c0);  // a multiple of 4
+    TreeAcc2 tr0, tr1;
+    tr0.init();
+    tr1.init();
+    // node n's sum: its L ranks in ring order from local rank `rot`
+    auto node = [&](int nb, uint64_t& n0, uint64_t& n1) {
+        if constexpr (LC == 1) {
+            const uint32_t wx = ld_shared_u32(base + nb * row + off) ^ 0x80808080u;
+            const uint64_t s2 = pk(sc[nb], sc[nb]);
+            n0 = fma2(sub2(pk(code_biased(wx, 0), code_biased(wx, 1)), C2), s2, z2);
+            n1 = fma2(sub2(pk(code_biased(wx, 2), code_biased(wx, 3)), C2), s2, z2);
+            return;
+        } else if constexpr (LC > 1) {
+#pragma unroll
+            for (int k = 0; k < LC; ++k) {
+                int r = rot + k;
+                r -= r >= LC ? LC : 0;
+                const uint32_t wx = ld_shared_u32(base + (nb + r) * row + off) ^ 0x80808080u;
                 const float s = sc[nb + r];
-                const uint64_t p0 = fma2(sub2(pk(code_biased(wx, 0), code_biased(wx, 1)), C2), pk(s, s), z2);
+                const uint64_t s2 = pk(s, s);
+                const uint64_t p0 = fma2(sub2(pk(code_biased(wx, 0), code_biased(wx, 1)), C2), s2, z2);
+                const uint64_t p1 = fma2(sub2(pk(code_biased(wx, 2), code_biased(wx, 3)), C2), s2, z2);
                 n0 = k == 0 ? p0 : add2(n0, p0);
-                r = r + 1 == L ? 0 : r + 1;
+                n1 = k == 0 ? p1 : add2(n1, p1);
             }
-            tr.push(n0);
+            return;
         }
-        float o0, o1;
-        unpk(tr.result(), o0, o1);
-        o0 = mean_of(o0, W, P.invW, pow2);
-        o1 = mean_of(o1, W, P.invW, pow2);
-        if (f0 >= a && f0 + 2 <= b) {
-            *reinterpret_cast<float2*>(P.out + f0) = make_float2(o0, o1);
-        } else {
-            if (f0 >= a && f0 < b) P.out[f0] = o0;
-            if (f0 + 1 >= a && f0 + 1 < b) P.out[f0 + 1] = o1;
+        int r = rot;
+        for (int k = 0; k < L; ++k) {
+            const uint32_t wx = ld_shared_u32(base + (nb + r) * row + off) ^ 0x80808080u;
+            const float s = sc[nb + r];
+            const uint64_t s2 = pk(s, s);
+            const uint64_t p0 = fma2(sub2(pk(code_biased(wx, 0), code_biased(wx, 1)), C2), s2, z2);
+            const uint64_t p1 = fma2(sub2(pk(code_biased(wx, 2), code_biased(wx, 3)), C2), s2, z2);
+            n0 = k == 0 ? p0 : add2(n0, p0);
+            n1 = k == 0 ? p1 : add2(n1, p1);
+            r = r + 1 == L ? 0 : r + 1;
         }
+    };
+    if constexpr (NODES > 0) {
+#pragma unroll
+        for (int n = 0; n < NODES; ++n) {
+            uint64_t n0 = 0, n1 = 0;
+            node(n * L, n0, n1);
+            tr0.push(n0);
+            tr1.push(n1);
+        }
+    } else {
+        for (int nb = 0; nb < W; nb += L) {
+            uint64_t n0 = 0, n1 = 0;
+            node(nb, n0, n1);
+            tr0.push(n0);
+            tr1.push(n1);
+        }
+    }
+    float o[4];
+    unpk(tr0.result(), o[0], o[1]);
+    unpk(tr1.result(), o[2], o[3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[e] = mean_of(o[e], W, P.invW, pow2);
+    if (f0 >= a && f0 + 4 <= b) {
+        *reinterpret_cast<float4*>(P.out + f0) = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (f0 + e >= a && f0 + e < b) P.out[f0 + e] = o[e];
     }
 }
 
-// HIER: the hierarchical-order build of the kernel (its own register allocation); the other
-// build takes the sequential, ring and tree orders.
-template <bool HIER>
+// The unit's words under a tree-like order, dispatched on the node count.
+template <int NODES, int LC>
+__device__ __forceinline__ void reduce_unit_hier(const PArgs& P, const unsigned char* base, uint32_t row,
+                                                const float* sc, int W, int L, int rot, int64_t c0, int64_t a,
+                                                int64_t b, bool pow2, int rtid) {
+#ifndef GQ_PIPE_HIER_UNROLL
+#define GQ_PIPE_HIER_UNROLL 1
+#endif
+    constexpr int kU = GQ_PIPE_HIER_UNROLL;
+#pragma unroll kU
+    for (int64_t w = a / 4 + rtid; w < (b + 3) / 4; w += kRThreads)
+        reduce_word4_hier<NODES, LC>(P, base, row, sc, W, L, rot, w, c0, a, b, pow2);
+}
+
+// Reducer kinds, one build of the kernel each (each with its own register allocation).
+constexpr int kRedLinear = 0;  // the sequential and ring orders
+constexpr int kRedTree = 1;    // the tree order (one-rank nodes)
+constexpr int kRedHier = 2;    // the hierarchical order
+template <int RED>
 __device__ void reducer(const PArgs& P, Shared& S, const unsigned char* rbuf, uint64_t limit, int rtid) {
     const int lane = rtid & 31;
     const int W = P.q.W;
     const uint32_t row = static_cast<uint32_t>(r_row(W));
     const bool pow2 = P.w_pow2 != 0;
-    const bool tree = P.order == fused::kOrderTree;
     const int L = P.hier_L;
     for (uint32_t useq = 0;; ++useq) {
         const uint32_t buf = useq & 1u;
@@ -964,12 +1002,32 @@ __device__ void reducer(const PArgs& P, Shared& S, const unsigned char* rbuf, ui
         const int rot = ri.rot;
         const unsigned char* base = rbuf + buf * kRBufBytes;
         const int64_t G0 = a / 16, G1 = (b + 15) / 16;
-        for (int64_t G = G0 + rtid; G < G1; G += kRThreads) {
-            if (HIER)
-                reduce_group16_hier(P, base, row, ri.s, W, L, rot, G * 16, c0, a, b, pow2);
-            else if (tree)
-                reduce_group16_tree(P, base, row, ri.s, W, G * 16, c0, a, b, pow2);
-            else
+        if (RED != kRedLinear) {
+            // power-of-two shapes up to W = 16 at compile time (node count, and node size)
+#define GQ_HIER_CASE(N, LCV) reduce_unit_hier<N, LCV>(P, base, row, ri.s, W, L, rot, c0, a, b, pow2, rtid)
+            if (RED == kRedTree) {
+                switch (W) {
+                    case 2: GQ_HIER_CASE(2, 1); break;
+                    case 4: GQ_HIER_CASE(4, 1); break;
+                    case 8: GQ_HIER_CASE(8, 1); break;
+                    case 16: GQ_HIER_CASE(16, 1); break;
+                    default: GQ_HIER_CASE(0, 1); break;
+                }
+            } else {
+                switch (W * 100 + L) {
+                    case 402: GQ_HIER_CASE(2, 2); break;
+                    case 802: GQ_HIER_CASE(4, 2); break;
+                    case 804: GQ_HIER_CASE(2, 4); break;
+                    case 808: GQ_HIER_CASE(1, 8); break;
+                    case 1602: GQ_HIER_CASE(8, 2); break;
+                    case 1604: GQ_HIER_CASE(4, 4); break;
+                    case 1608: GQ_HIER_CASE(2, 8); break;
+                    default: GQ_HIER_CASE(0, 0); break;
+                }
+            }
+#undef GQ_HIER_CASE
+        } else {
+            for (int64_t G = G0 + rtid; G < G1; G += kRThreads)
                 reduce_group16(P, base, row, ri.s, W, rot, G * 16, c0, a, b, pow2);
         }
         // the code lines of every rank wholly inside [a, b) were read for the last time by this
@@ -985,7 +1043,7 @@ __device__ void reducer(const PArgs& P, Shared& S, const unsigned char* rbuf, ui
 
 // ----------------------------------------------------------------------------- kernel
 
-template <int DT, bool HIER>
+template <int DT, int RED>
 __global__ void __launch_bounds__(kThreads, 1) k_pipe(const PArgs P) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Shared S;
@@ -1022,7 +1080,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pipe(const PArgs P) {
     } else if (warp < 2 + kQWarps) {
         quantiser<DT>(P, S, ring, tag, limit, tid - 64);
     } else {
-        reducer<HIER>(P, S, rbuf, limit, tid - 64 - kQThreads);
+        reducer<RED>(P, S, rbuf, limit, tid - 64 - kQThreads);
     }
     __syncthreads();
 
@@ -1066,18 +1124,16 @@ inline void init_pipe(PipeInit* pi) {
     int per_sm = 0, sms = 0, dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    int per_sm_h = 0;
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_pipe<DT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_pipe<DT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_pipe<DT, false>, kThreads, kSmemBytes);
-    if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_h, k_pipe<DT, true>, kThreads, kSmemBytes);
-    if (per_sm_h < per_sm) per_sm = per_sm_h;
+    // the three builds share the launch shape; take the smallest residency of the three
+    const void* fns[3] = {reinterpret_cast<const void*>(k_pipe<DT, kRedLinear>),
+                          reinterpret_cast<const void*>(k_pipe<DT, kRedTree>),
+                          reinterpret_cast<const void*>(k_pipe<DT, kRedHier>)};
+    for (int f = 0; f < 3 && e == cudaSuccess; ++f) {
+        int n = 0;
+        e = cudaFuncSetAttribute(fns[f], cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fns[f], kThreads, kSmemBytes);
+        if (e == cudaSuccess && (f == 0 || n < per_sm)) per_sm = n;
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         pi->err = e;
@@ -1103,8 +1159,9 @@ inline cudaError_t launch_pipe_dt(PipeInit* table, const QuantArgs& a, int order
     PArgs P;
     P.q = a;
     P.order = order;
-    P.hier_L = order > kOrderHierBase ? order - kOrderHierBase : 0;
-    P.nseg = P.hier_L > 0 ? P.hier_L : a.W;
+    // tree-like orders: nodes of hier_L ranks (one-rank nodes for the tree order)
+    P.hier_L = order > kOrderHierBase ? order - kOrderHierBase : order == fused::kOrderTree ? 1 : 0;
+    P.nseg = order > kOrderHierBase ? P.hier_L : a.W;
     P.out = out;
     P.codes_out = codes;
     P.scales_out = scales;
@@ -1125,10 +1182,12 @@ inline cudaError_t launch_pipe_dt(PipeInit* table, const QuantArgs& a, int order
     if (want > static_cast<unsigned long long>(pi.ctas)) want = static_cast<unsigned long long>(pi.ctas);
     if (max_ctas > 0 && want > static_cast<unsigned long long>(max_ctas)) want = static_cast<unsigned long long>(max_ctas);
     const unsigned grid = static_cast<unsigned>(want);
-    if (P.hier_L > 0)
-        k_pipe<DT, true><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    if (order == fused::kOrderTree)
+        k_pipe<DT, kRedTree><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    else if (P.hier_L > 0)
+        k_pipe<DT, kRedHier><<<grid, kThreads, kSmemBytes, stream>>>(P);
     else
-        k_pipe<DT, false><<<grid, kThreads, kSmemBytes, stream>>>(P);
+        k_pipe<DT, kRedLinear><<<grid, kThreads, kSmemBytes, stream>>>(P);
     return cudaGetLastError();
 }
 
