@@ -283,3 +283,38 @@ def test_pipe_copy_wait_runs_out_and_is_reported():
     assert gq.gq_get_error() == gq.GQ_OK
     want = oracle.fused(host, W, stride, d_off.cpu().numpy(), oracle.RING)[0]
     H.assert_bits_equal(out.cpu().numpy(), want, "output after the timeout")
+
+
+@pytest.mark.parametrize("world", [3])
+def test_pipe_sharded_table(world):
+    """The multi-GPU split run on one GPU: each shard's sub-table (global offsets) through the
+    pipelined call and the two-kernel path writes its own output range; together they are the
+    unsplit result, bit for bit."""
+    from dp_gradient_bucket_gb300 import shard
+    W = 8
+    buckets = [5, 65535, 131075, 7, 32769 * 3 + 1, 3, 49152]
+    off = oracle.plan_chunks(buckets, 4)
+    n = int(off[-1])
+    stride = gq.row_stride(n, 4)
+    host = np.zeros(W * stride, dtype=np.float32)
+    for r in range(W):
+        wl.fill(2, r, 0, n, host[r * stride:r * stride + n])
+    dev = torch.device("cuda:0")
+    grads = torch.from_numpy(host).to(dev)
+    want = oracle.fused(host, W, stride, off, oracle.RING)[0]
+    out = torch.zeros(n, dtype=torch.float32, device=dev)
+    out2 = torch.zeros(n, dtype=torch.float32, device=dev)
+    codes = torch.zeros(W * stride, dtype=torch.int8, device=dev)
+    for rank in range(world):
+        sub, k = shard.shard_table(off, world, rank)
+        if k == 0:
+            continue
+        d_sub = torch.from_numpy(sub).to(dev)
+        ws = _ws(W, stride, k, dev)
+        gq.gq_fused_allreduce_sim_pipelined(grads, W, stride, d_sub, k, 1.0, "ring", out, ws)
+        scales = torch.zeros(W * k, dtype=torch.float32, device=dev)
+        gq.gq_quantize(grads, W, stride, d_sub, k, 1.0, codes, scales)
+        gq.gq_reduce_dequant(codes, scales, W, stride, d_sub, k, "ring", out2)
+    assert gq.gq_get_error() == gq.GQ_OK
+    H.assert_bits_equal(out.cpu().numpy(), want, "pipelined, sharded")
+    H.assert_bits_equal(out2.cpu().numpy(), want, "two-kernel, sharded")
