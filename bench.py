@@ -49,7 +49,7 @@ def parse():
     p.add_argument("--impl", default="gq", choices=["gq", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample length (cpu_baseline)")
     p.add_argument("--bwd-k", type=int, default=512, help="inner size of the synthetic backward GEMM (--sweep overlap)")
-    p.add_argument("--sweep", default=None, choices=["chunk", "order", "scope", "adaptive", "overlap"],
+    p.add_argument("--sweep", default=None, choices=["chunk", "order", "scope", "adaptive", "overlap", "workloads"],
                    help="instead of the headline line: one JSON line per base chunk size (chunk), summation "
                         "order (order) or scale scope (scope) of the pipelined kernel on the headline bucket, or "
                         "the adaptive chunk-size chooser run online (adaptive)")
@@ -647,12 +647,96 @@ def run_overlap(args):
         print(json.dumps(r), flush=True)
 
 
+def run_workloads(args):
+    """The pipelined kernel on every synthetic workload: W = 2 x 1 MiB (seq), the 25 MiB bucket,
+    the ResNet-152 gradient set in 25 MiB buckets, BERT-Large fp16 at W = 16 (loss scale 65536),
+    and W = 8 buckets of 4 KiB to 1 GiB (ring).  One launch covers a workload's whole chunk table.
+    Rows are generated on the host up to 32 Mi elements per rank and repeated on the device beyond
+    that (same value distribution).  Inputs smaller than L2 stay L2-resident between launches:
+    those lines are latency figures, not roofline."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import dp_gradient_bucket_gb300 as gq
+    import workloads as wl
+    import oracle  # bucket assignment of the tensor-list workloads (host planning only)
+    peak = float(measured_peaks()[0]["hbm_gbs"])
+    stream = torch.cuda.current_stream(dev)
+    l2_bytes = 129 * 10 ** 6
+    gen_cap = 32 << 20
+
+    def device_rows(cfg, W, n):
+        dt = torch.float16 if wl.np_dtype(cfg) == np.float16 else torch.float32
+        eb = 2 if dt == torch.float16 else 4
+        stride = wl.row_stride(n, eb)
+        rows = torch.zeros(W, stride, dtype=dt, device=dev)
+        m = min(n, gen_cap)
+        for r in range(W):
+            block = torch.from_numpy(wl.fill(cfg, r, 0, m)).to(dev)
+            for s0 in range(0, n, m):
+                k = min(m, n - s0)
+                rows[r, s0:s0 + k] = block[:k]
+        return rows.view(-1), stride, eb
+
+    def measure(name, cfg, W, buckets, order, loss_scale, reps):
+        n = int(sum(buckets))
+        grads, stride, eb = device_rows(cfg, W, n)
+        nc = gq.gq_plan_chunks(buckets, eb)
+        off = torch.empty(nc + 1, dtype=torch.int64, device=dev)
+        gq.gq_plan_chunks(buckets, eb, off, stream)
+        out = torch.empty(max(n, 4), dtype=torch.float32, device=dev)
+        ws = torch.zeros(gq.gq_pipelined_workspace_bytes(W, stride, nc), dtype=torch.uint8, device=dev)
+        call = lambda: gq.gq_fused_allreduce_sim_pipelined(grads, W, stride, off, nc, loss_scale, order, out, ws,
+                                                            stream=stream)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record(stream)
+            call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        st = gq.gq_get_error(stream)
+        if st != gq.GQ_OK:
+            raise RuntimeError("%s: %s" % (name, gq.gq_status_string(st)))
+        us = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+        avg = sum(us) / len(us)
+        in_bytes = W * n * eb
+        row = {"sweep": "workloads", "workload": name, "W": W, "dtype": "f16" if eb == 2 else "f32",
+               "elements_per_rank": n, "buckets": len(buckets), "chunks": nc, "order": order,
+               "kernel_avg_us": avg, "kernel_median_us": us[len(us) // 2],
+               "input_gbs": in_bytes / (avg * 1e-6) / 1e9,
+               "roofline_frac": (in_bytes + 4 * n) / (avg * 1e-6) / 1e9 / peak,
+               "l2_resident": in_bytes + 4 * n < l2_bytes, "peak_gbs": peak}
+        print(json.dumps(row), flush=True)
+        del grads, out, ws
+        torch.cuda.empty_cache()
+
+    measure("W=2 x 1 MiB fp32 (8 chunks), seq", 1, 2, [262144], "seq", 1.0, 200)
+    measure("W=8 x 25 MiB fp32 bucket, ring", 2, 8, [N_ELEMS], "ring", 1.0, 200)
+    for cfg, W, eb, name in ((3, 8, 4, "W=8 ResNet-152 gradient set (60.2 M fp32 per rank), 25 MiB buckets, ring"),
+                             (4, 16, 2, "W=16 BERT-Large fp16 (335 M per rank), loss scale 65536, 25 MiB buckets, ring")):
+        sizes, _ = wl.tensor_layout(cfg)
+        buckets = [int(x) for x in oracle.assign_buckets([int(x) for x in sizes], eb)[1]]
+        measure(name, cfg, W, buckets, "ring", 65536.0 if cfg == 4 else 1.0, 20)
+    for k in range(10, 29, 2):
+        n = 2 ** k
+        measure("W=8 one %s fp32 bucket, ring" % ("%d KiB" % (4 * n // 1024) if n < 2 ** 18 else
+                                                  "%d MiB" % (4 * n // 2 ** 20)), 5, 8, [n], "ring", 1.0,
+                200 if n <= 2 ** 20 else 20)
+    for n in (2 ** 20 + 17, 1000003):
+        measure("W=8 one fp32 bucket of %d elements, ring" % n, 5, 8, [n], "ring", 1.0, 200)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
     elif args.sweep == "overlap":
         run_overlap(args)
+    elif args.sweep == "workloads":
+        run_workloads(args)
     elif args.sweep:
         run_sweep(args)
     else:

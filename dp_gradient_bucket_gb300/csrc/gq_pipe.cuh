@@ -38,7 +38,12 @@ using fused::mean_of;
 using fused::raise_error;
 using fused::store_codes;
 
-constexpr int kPiece = 16384;  // bytes per bulk copy and per ring slot
+constexpr int kPiece = 16384;  // bytes per bulk copy
+// A rank-chunk of slightly more than a whole number of pieces (dynamic_chunk's pieces are often up
+// to a few hundred elements over 128 KiB) would end in a piece of a few bytes: it is merged into the
+// piece before, so a slot holds up to kPiece + kPieceSlack bytes.
+constexpr int kPieceSlack = 1024;
+constexpr int kSlotBytes = kPiece + kPieceSlack;
 #ifndef GQ_PIPE_SLOTS
 #define GQ_PIPE_SLOTS 11
 #endif
@@ -59,14 +64,15 @@ constexpr int kInfo = 16;  // item descriptors in flight (> kSlots)
 constexpr int kGroupsPerPiece = kPiece / 16;
 constexpr int kQBar = 1;   // named barrier of the quantisers (0 is __syncthreads)
 // Reduce buffers: two, each holding one reduce unit's codes of every rank, a row per rank.  A unit
-// is at most r_unit(W) elements of one ring segment; its row holds the 16-byte-aligned bytes that
-// cover it (at most r_unit(W) + 32).
+// of one ring segment is copied from the L2 line holding its first code; it ends on the 128-element
+// grid after r_unit(W) elements of that line, except the segment's last unit, which takes the rest
+// when that fits a row (up to r_unit_max(W) codes from the line start).
 #ifndef GQ_PIPE_RBUF_CODES
 #define GQ_PIPE_RBUF_CODES 16384
 #endif
 constexpr int kRBufCodes = GQ_PIPE_RBUF_CODES;
-// A unit of E elements (E a multiple of 128) starting anywhere is copied from its 16-byte-aligned
-// start to its 16-byte-aligned end: at most E + 16 bytes per row.
+// Headroom of kRSlack bytes per possible rank on top of kRBufCodes: with it a rank's row holds more
+// than r_unit(W) codes, room for a segment's last unit (r_unit_max below).
 #ifndef GQ_PIPE_RSLACK
 #define GQ_PIPE_RSLACK 16
 #endif
@@ -74,8 +80,17 @@ constexpr int kRSlack = GQ_PIPE_RSLACK;
 static_assert(kRSlack >= 16 && kRSlack % 16 == 0, "row slack");
 static_assert(kRBufCodes / kMaxRanks >= 128, "a reduce unit must hold at least 128 elements at W = 64");
 constexpr int kRBufBytes = kRBufCodes + kMaxRanks * kRSlack;
-constexpr size_t kSmemBytes = static_cast<size_t>(kSlots) * kPiece + 2 * kRBufBytes;
+constexpr size_t kSmemBytes = static_cast<size_t>(kSlots) * kSlotBytes + 2 * kRBufBytes;
+
+// Pieces of an item of `bytes` bytes: whole pieces of kPiece, the last one taking a remainder of
+// at most kPieceSlack bytes instead of a piece of its own.
+__host__ __device__ __forceinline__ int pieces_of(int64_t bytes) {
+    int64_t np = (bytes + kPiece - 1) / kPiece;
+    if (np > 1 && bytes - (np - 1) * kPiece <= kPieceSlack) --np;
+    return static_cast<int>(np);
+}
 static_assert(kInfo > kSlots, "an item descriptor must outlive the pieces issued after it");
+static_assert(kSmemBytes + 4096 <= 232448, "dynamic shared memory plus the static part within 227 KiB");
 // Each piece is worked on by a pair of quantiser warps, each taking half of its groups; piece p of an
 // item goes to pair p % kPairs, so a warp waits for, and hands back, only its own pieces.
 constexpr int kWarpsPerPiece = 2;
@@ -96,10 +111,14 @@ constexpr int kTwoPassPieces = GQ_PIPE_TWOPASS_PIECES;
 static_assert(kTwoPassPieces >= 1 && kTwoPassPieces <= kSlots + 1, "two-pass threshold");
 static_assert(kThreads <= 1024, "block size");
 
-// Elements per reduce unit for W ranks: a multiple of 128 (so units of an aligned segment start on
-// L2 lines) with W rows of codes in kRBufCodes bytes.
+// Elements per reduce unit for W ranks: a multiple of 128 with W rows of codes in kRBufCodes bytes.
+// A rank's row is the buffer's W-th part (a 16-byte multiple), so a segment's last unit may run on
+// to r_unit_max(W) codes (the row less 16 bytes of alignment): a segment a little longer than a
+// multiple of r_unit(W), as dynamic_chunk's pieces often give, needs no extra unit for its end.
 __host__ __device__ __forceinline__ int r_unit(int W) { return (kRBufCodes / W) / 128 * 128; }
-__host__ __device__ __forceinline__ int r_row(int W) { return r_unit(W) + kRSlack; }
+__host__ __device__ __forceinline__ int r_row(int W) { return (kRBufBytes / W) / 16 * 16; }
+__host__ __device__ __forceinline__ int r_unit_max(int W) { return r_row(W) - 16; }
+static_assert((kRBufBytes / kMaxRanks) / 16 * 16 - 16 >= kRBufCodes / kMaxRanks / 128 * 128, "unit fits a row");
 
 // Workspace: a 256-byte header, one 64-bit word per (chunk, rank) at j * W + r, then the codes,
 // W rows of cstride bytes (cstride = rank_stride rounded up to 128, so rows start on L2 lines).
@@ -369,9 +388,15 @@ __device__ void producer(const PArgs& P, Shared& S, unsigned char* ring, uint32_
             item = next;
             continue;
         }
-        const int64_t g0 = lo / VEC, g1 = (hi + VEC - 1) / VEC;
+        // the copy starts at the 128-byte line that holds the chunk's first group: up to 7 groups of
+        // the row before the chunk ride along (masked out like any group outside the chunk), so the
+        // bulk copies read whole lines whatever the chunk's offset
+        const char* row = grads + r * row_bytes;
+        const int64_t gc = lo / VEC;
+        const int64_t lead = static_cast<int64_t>((reinterpret_cast<uintptr_t>(row) / 16 + static_cast<uint64_t>(gc)) % 8);
+        const int64_t g0 = gc - (lead < gc ? lead : gc), g1 = (hi + VEC - 1) / VEC;
         const int64_t bytes = (g1 - g0) * 16;
-        const int np = static_cast<int>((bytes + kPiece - 1) / kPiece);
+        const int np = pieces_of(bytes);
         const int twopass = np >= kTwoPassPieces ? 1 : 0;
         Info& in = S.info[k % kInfo];
         in.lo = lo;
@@ -383,7 +408,7 @@ __device__ void producer(const PArgs& P, Shared& S, unsigned char* ring, uint32_
         in.np = np;
         in.twopass = twopass;
         in.valid = 1;
-        const char* src = grads + r * row_bytes + g0 * 16;
+        const char* src = row + g0 * 16;
         for (int pass = 0; pass <= twopass && ok; ++pass) {
             for (int p = 0; p < np; ++p) {
                 if (!acquire(seq)) {
@@ -392,11 +417,11 @@ __device__ void producer(const PArgs& P, Shared& S, unsigned char* ring, uint32_
                 }
                 const uint32_t slot = seq % kSlots;
                 const int64_t left = bytes - static_cast<int64_t>(p) * kPiece;
-                const uint32_t nb = static_cast<uint32_t>(left < kPiece ? left : kPiece);
+                const uint32_t nb = static_cast<uint32_t>(p == np - 1 ? left : kPiece);  // left <= kSlotBytes
                 st_release_shared_u32(&S.slot_seq[slot], seq);  // after the descriptor, before the arrival
                 mbar_arrive_expect_tx(&S.full[slot], nb + extra);
                 extra = 0;
-                bulk_copy_g2s_hint(ring + static_cast<size_t>(slot) * kPiece, src + static_cast<int64_t>(p) * kPiece, nb,
+                bulk_copy_g2s_hint(ring + static_cast<size_t>(slot) * kSlotBytes, src + static_cast<int64_t>(p) * kPiece, nb,
                                    &S.full[slot], (twopass && pass == 0) ? again : once);
                 S.issued[slot] += 1u;
                 ++seq;
@@ -471,6 +496,14 @@ __device__ __forceinline__ void quantise_group(const V16& v, uint64_t c2, uint64
     }
 }
 
+// Groups of piece p that warp `half` of its pair takes, starting at group gp: half a piece each, the
+// second half of the last piece also taking the merged remainder (at most kPieceSlack / 16 groups).
+__device__ __forceinline__ uint32_t half_groups(int p, int np, uint32_t half, uint32_t gp, uint32_t ngroups) {
+    const uint32_t pend = p == np - 1 ? ngroups : min(ngroups, static_cast<uint32_t>(p + 1) * kGroupsPerPiece);
+    if (gp >= pend) return 0u;
+    return half == 0 ? min(static_cast<uint32_t>(kHalfGroups), pend - gp) : pend - gp;
+}
+
 template <int DT>
 __device__ void quantiser(const PArgs& P, Shared& S, const unsigned char* ring, uint32_t tag, uint64_t limit,
                           int qtid) {
@@ -511,10 +544,11 @@ __device__ void quantiser(const PArgs& P, Shared& S, const unsigned char* ring, 
 
         // ---- pass A: absmax over the rank-chunk
         // groups are numbered from the item's first (32-bit); groups [gf0, gf0 + gfull) lie wholly
-        // inside the chunk, only the first and the last can stick out of it
+        // inside the chunk, the leading ones (up to 8, from the line alignment) and the last one can
+        // lie partly or wholly outside it
         const uint32_t ngroups = static_cast<uint32_t>(in.bytes / 16);
-        const uint32_t gf0 = (in.lo % VEC) != 0 ? 1u : 0u;
-        const uint32_t gend = ngroups - ((in.hi % VEC) != 0 ? 1u : 0u);
+        const uint32_t gf0 = static_cast<uint32_t>((in.lo + VEC - 1) / VEC - in.g0);  // first whole group
+        const uint32_t gend = static_cast<uint32_t>(in.hi / VEC - in.g0);             // past the last whole one
         const uint32_t gfull = gend > gf0 ? gend - gf0 : 0u;
         float mf = 0.0f;
         uint32_t mi = 0;
@@ -526,8 +560,8 @@ __device__ void quantiser(const PArgs& P, Shared& S, const unsigned char* ring, 
                 break;
             }
             const uint32_t gp = static_cast<uint32_t>(p) * kGroupsPerPiece + half * kHalfGroups;  // this warp's first
-            const uint32_t ng = gp < ngroups ? min(static_cast<uint32_t>(kHalfGroups), ngroups - gp) : 0u;
-            const unsigned char* base = ring + static_cast<size_t>(slot) * kPiece + half * (kHalfGroups * 16);
+            const uint32_t ng = half_groups(p, in.np, half, gp, ngroups);
+            const unsigned char* base = ring + static_cast<size_t>(slot) * kSlotBytes + half * (kHalfGroups * 16);
             if (DT == 0 && ng == kHalfGroups && gp - gf0 < gfull && gp + ng <= gf0 + gfull) {
                 // a full half-piece of whole groups: a fixed share per lane, no tests
 #pragma unroll 8
@@ -599,8 +633,8 @@ __device__ void quantiser(const PArgs& P, Shared& S, const unsigned char* ring, 
                 break;
             }
             const uint32_t gp = static_cast<uint32_t>(p) * kGroupsPerPiece + half * kHalfGroups;
-            const uint32_t ng = gp < ngroups ? min(static_cast<uint32_t>(kHalfGroups), ngroups - gp) : 0u;
-            const unsigned char* base = ring + static_cast<size_t>(slot) * kPiece + half * (kHalfGroups * 16);
+            const uint32_t ng = half_groups(p, in.np, half, gp, ngroups);
+            const unsigned char* base = ring + static_cast<size_t>(slot) * kSlotBytes + half * (kHalfGroups * 16);
             if (ng == kHalfGroups && gp - gf0 < gfull && gp + ng <= gf0 + gfull && !urow) {
                 // a full half-piece of whole groups, codes to the workspace only
 #pragma unroll kUnrollB
@@ -668,7 +702,7 @@ static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf,
     const int64_t n = P.q.num_chunks;
     const bool ring = P.order == fused::kOrderRing;
     const int L = P.hier_L;
-    const int64_t E = r_unit(W);
+    const int64_t E = r_unit(W), Emax = r_unit_max(W);
     const uint32_t row = static_cast<uint32_t>(r_row(W));
     const uint64_t once = l2_policy_evict_first();
     uint32_t useq = 0;  // units handed over
@@ -735,14 +769,16 @@ static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf,
         fence_acq_rel_gpu();         // acquire: the codes stored before the words
         fence_proxy_async_global();  // ... and before the bulk copies that read them
         const int rot = ring ? (t + 1 == W ? 0 : t + 1) : L > 0 ? (t + 1) % L : 0;
-        for (int64_t x = a; x < b; x += E) {
+        for (int64_t x = a; x < b;) {
             if (!acquire(useq)) {
                 ok = false;
                 break;
             }
             const uint32_t buf = useq & 1u;
-            const int64_t xb = min(b, x + E);
-            const int64_t c0 = x & ~static_cast<int64_t>(15);
+            // the copy starts on an L2 line; the unit ends on the 128-element grid, or, for the
+            // segment's last unit, at the segment's end
+            const int64_t c0 = x & ~static_cast<int64_t>(127);
+            const int64_t xb = b - c0 <= Emax ? b : c0 + E;
             const uint32_t nb = static_cast<uint32_t>(((xb + 15) & ~static_cast<int64_t>(15)) - c0);
             RInfo& ri = S.rinfo[buf];
             if (lane == 0) {
@@ -763,6 +799,7 @@ static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf,
                                    once);
             if (lane == 0) S.rissued[buf] += 1u;
             ++useq;
+            x = xb;
         }
         if (!ok) {
             fail_now();
@@ -1048,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pipe(const PArgs P) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ Shared S;
     unsigned char* ring = smem;
-    unsigned char* rbuf = smem + static_cast<size_t>(kSlots) * kPiece;
+    unsigned char* rbuf = smem + static_cast<size_t>(kSlots) * kSlotBytes;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         for (int s = 0; s < kSlots; ++s) {
