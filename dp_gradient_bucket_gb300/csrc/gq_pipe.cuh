@@ -123,8 +123,8 @@ static_assert((kRBufBytes / kMaxRanks) / 16 * 16 - 16 >= kRBufCodes / kMaxRanks 
 // Workspace: a 256-byte header, one 64-bit word per (chunk, rank) at j * W + r, then the codes,
 // W rows of cstride bytes (cstride = rank_stride rounded up to 128, so rows start on L2 lines).
 struct Hdr {
-    unsigned long long q_head;  // next quantise item
-    unsigned long long r_head;  // next reduce item
+    unsigned long long q_head;  // quantise items claimed past the first of each CTA
+    unsigned long long r_head;  // reduce items claimed past the first of each CTA
     unsigned exit_count;        // CTAs of this launch that have left
     unsigned epoch;             // launches completed (mod 2^32 - 1): the tag is epoch + 1
 };
@@ -371,9 +371,11 @@ __device__ void producer(const PArgs& P, Shared& S, unsigned char* ring, uint32_
         st_volatile_int(&S.abort, 1);
         return false;
     };
-    unsigned long long item = atomicAdd(&P.hdr->q_head, 1ull);
+    // the first item of CTA b is item b (the grid never exceeds the quantise items); later ones are
+    // claimed from the counter, numbered from gridDim.x
+    unsigned long long item = blockIdx.x;
     while (item < P.total_q && !ld_volatile_int(&S.abort)) {
-        const unsigned long long next = atomicAdd(&P.hdr->q_head, 1ull);  // used after this item
+        const unsigned long long next = gridDim.x + atomicAdd(&P.hdr->q_head, 1ull);  // used after this item
         const int64_t j = static_cast<int64_t>(item / W);
         const int r = static_cast<int>(item % W);
         int64_t lo, hi;
@@ -717,19 +719,17 @@ static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf,
         if (u < 2u) return true;
         return warp_wait_slot(&S.rempty[u & 1u], ((u >> 1) - 1u) & 1u, limit, &S.abort);
     };
-    unsigned long long item = 0, next = 0;
-    if (lane == 0) {
-        item = atomicAdd(&P.hdr->r_head, 1ull);
-        next = atomicAdd(&P.hdr->r_head, 1ull);
-    }
-    item = __shfl_sync(0xffffffffu, item, 0);
+    // the first reduce item of CTA b is item b; later ones are claimed from the counter, numbered from
+    // gridDim.x
+    unsigned long long item = blockIdx.x, next = 0;
+    if (lane == 0) next = gridDim.x + atomicAdd(&P.hdr->r_head, 1ull);
     for (;;) {
         if (item >= P.total_r || ld_volatile_int(&S.abort)) break;
         const int64_t j = static_cast<int64_t>(item / US);
         const int t = static_cast<int>(item % US);
         // claim the item after next now: its latency hides behind this one
         unsigned long long after = 0;
-        if (lane == 0) after = atomicAdd(&P.hdr->r_head, 1ull);
+        if (lane == 0) after = gridDim.x + atomicAdd(&P.hdr->r_head, 1ull);
         item = __shfl_sync(0xffffffffu, next, 0);
         next = after;
         int64_t lo, hi;
@@ -1088,6 +1088,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_pipe(const PArgs P) {
     unsigned char* rbuf = smem + static_cast<size_t>(kSlots) * kSlotBytes;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
+        // the epoch moves only after every CTA of this launch has left, so all CTAs read one value; the
+        // load is issued first, its latency hidden behind the barrier set-up
+        const unsigned epoch = *reinterpret_cast<volatile unsigned*>(&P.hdr->epoch);
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(&S.full[s], 1);
             mbar_init(&S.empty[s], kWarpsPerPiece);
@@ -1102,8 +1105,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_pipe(const PArgs P) {
         fence_barrier_init();
         S.abort = 0;
         S.last = 0;
-        // the epoch moves only after every CTA of this launch has left, so all CTAs read one value
-        S.tag = *reinterpret_cast<volatile unsigned*>(&P.hdr->epoch) + 1u;
+        S.tag = epoch + 1u;
     }
     __syncthreads();
     const uint32_t tag = S.tag;
