@@ -280,6 +280,13 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
     return r;
 }
 
+// Per 16-bit lane unsigned maximum of two packed pairs.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // max(m, |a|, |b|), NaN propagated (a NaN orders above every number in the final bit pattern).
 __device__ __forceinline__ float absmax3(float m, float a, float b) {
     float r;
@@ -572,6 +579,19 @@ __device__ void quantiser(const PArgs& P, Shared& S, const unsigned char* ring, 
                     mf = absmax3(mf, __uint_as_float(v.w[0]), __uint_as_float(v.w[1]));
                     mf = absmax3(mf, __uint_as_float(v.w[2]), __uint_as_float(v.w[3]));
                 }
+            } else if (DT == 1 && ng == kHalfGroups && gp - gf0 < gfull && gp + ng <= gf0 + gfull) {
+                // the same for binary16: the |x| bit patterns of two halves at a time (a packed
+                // unsigned 16-bit max keeps their order, NaN above +Inf)
+                uint32_t m2 = 0;
+#pragma unroll 8
+                for (int k = 0; k < kGroupsPerLane; ++k) {
+                    const V16 v = ld_shared_v16(base + (lane + 32 * k) * 16);
+                    m2 = max_u16x2(m2, v.w[0] & 0x7fff7fffu);
+                    m2 = max_u16x2(m2, v.w[1] & 0x7fff7fffu);
+                    m2 = max_u16x2(m2, v.w[2] & 0x7fff7fffu);
+                    m2 = max_u16x2(m2, v.w[3] & 0x7fff7fffu);
+                }
+                mi = max(mi, max(m2 & 0xffffu, m2 >> 16));
             } else {
 #pragma unroll 1
                 for (uint32_t gl = lane; gl < ng; gl += 32) {
