@@ -156,7 +156,7 @@ typedef enum { GQ_SCOPE_CHUNK = 0, GQ_SCOPE_BUCKET = 1, GQ_SCOPE_TENSOR = 2 } gq
  *                 (GQ_ERR_INVALID_ARG if that divisor is 0); ignored by the other scopes
  *   the rest      as gq_plan_chunks, which is gq_plan_chunks_ex(..., GQ_SCOPE_CHUNK, GQ_CHUNK_SIZE, ...).
  * The quantise and reduce calls take the table whatever the scope; chunks longer than the
- * pipelined kernel's shared-memory ring (176 KiB of input per rank) are read twice. */
+ * pipelined kernel's shared-memory ring (about 177 KiB of input per rank) are read twice. */
 gq_status gq_plan_chunks_ex(const size_t* elems, size_t count, size_t elem_bytes, gq_scope scope,
                             size_t chunk_bytes, int64_t* d_offsets, size_t offsets_capacity,
                             size_t* num_chunks_out, gq_stream_t stream);
