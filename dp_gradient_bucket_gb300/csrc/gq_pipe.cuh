@@ -120,6 +120,15 @@ __host__ __device__ __forceinline__ int r_row(int W) { return (kRBufBytes / W) /
 __host__ __device__ __forceinline__ int r_unit_max(int W) { return r_row(W) - 16; }
 static_assert((kRBufBytes / kMaxRanks) / 16 * 16 - 16 >= kRBufCodes / kMaxRanks / 128 * 128, "unit fits a row");
 
+// First code byte copied for the reduce unit that starts at element x (the L2 line holding it), and the
+// unit's end within the segment ending at b: the 128-element grid after r_unit(W) codes of the line,
+// or b when the rest fits a row.  Copies are [c0, round_up(end, 16)), at most r_row(W) bytes.
+__host__ __device__ __forceinline__ int64_t unit_copy_start(int64_t x) { return x & ~static_cast<int64_t>(127); }
+__host__ __device__ __forceinline__ int64_t unit_end(int64_t x, int64_t b, int W) {
+    const int64_t c0 = unit_copy_start(x);
+    return b - c0 <= r_unit_max(W) ? b : c0 + r_unit(W);
+}
+
 // Workspace: a 256-byte header, one 64-bit word per (chunk, rank) at j * W + r, then the codes,
 // W rows of cstride bytes (cstride = rank_stride rounded up to 128, so rows start on L2 lines).
 struct Hdr {
@@ -507,10 +516,11 @@ __device__ __forceinline__ void quantise_group(const V16& v, uint64_t c2, uint64
 
 // Groups of piece p that warp `half` of its pair takes, starting at group gp: half a piece each, the
 // second half of the last piece also taking the merged remainder (at most kPieceSlack / 16 groups).
-__device__ __forceinline__ uint32_t half_groups(int p, int np, uint32_t half, uint32_t gp, uint32_t ngroups) {
-    const uint32_t pend = p == np - 1 ? ngroups : min(ngroups, static_cast<uint32_t>(p + 1) * kGroupsPerPiece);
+__host__ __device__ __forceinline__ uint32_t half_groups(int p, int np, uint32_t half, uint32_t gp, uint32_t ngroups) {
+    const uint32_t end = static_cast<uint32_t>(p + 1) * kGroupsPerPiece;
+    const uint32_t pend = p == np - 1 ? ngroups : (ngroups < end ? ngroups : end);
     if (gp >= pend) return 0u;
-    return half == 0 ? min(static_cast<uint32_t>(kHalfGroups), pend - gp) : pend - gp;
+    return half == 0 ? (pend - gp < static_cast<uint32_t>(kHalfGroups) ? pend - gp : kHalfGroups) : pend - gp;
 }
 
 template <int DT>
@@ -724,7 +734,6 @@ static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf,
     const int64_t n = P.q.num_chunks;
     const bool ring = P.order == fused::kOrderRing;
     const int L = P.hier_L;
-    const int64_t E = r_unit(W), Emax = r_unit_max(W);
     const uint32_t row = static_cast<uint32_t>(r_row(W));
     const uint64_t once = l2_policy_evict_first();
     uint32_t useq = 0;  // units handed over
@@ -797,8 +806,8 @@ static __device__ void rproducer(const PArgs& P, Shared& S, unsigned char* rbuf,
             const uint32_t buf = useq & 1u;
             // the copy starts on an L2 line; the unit ends on the 128-element grid, or, for the
             // segment's last unit, at the segment's end
-            const int64_t c0 = x & ~static_cast<int64_t>(127);
-            const int64_t xb = b - c0 <= Emax ? b : c0 + E;
+            const int64_t c0 = unit_copy_start(x);
+            const int64_t xb = unit_end(x, b, W);
             const uint32_t nb = static_cast<uint32_t>(((xb + 15) & ~static_cast<int64_t>(15)) - c0);
             RInfo& ri = S.rinfo[buf];
             if (lane == 0) {

@@ -1,0 +1,91 @@
+"""Shared-memory geometry of the pipelined kernel, checked on the host against the kernel's own
+header (no GPU): every bulk copy fits the slot or row it lands in, pieces and reduce units tile their
+ranges exactly, and the two warps of a pair split each piece without overlap or gap.  A host program
+including gq_pipe.cuh is compiled with nvcc and run."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "dp_gradient_bucket_gb300", "csrc")
+
+PROGRAM = r'''
+#include <cstdio>
+#include <cstdint>
+#include "gq_pipe.cuh"
+using namespace gq::pipe;
+using gq::kMaxRanks;
+
+static uint64_t rng = 0x9E3779B97F4A7C15ull;
+static uint64_t next_u64() { rng ^= rng << 13; rng ^= rng >> 7; rng ^= rng << 17; return rng; }
+
+#define CHECK(c, ...) do { if (!(c)) { std::printf(__VA_ARGS__); std::printf("\n"); return 1; } } while (0)
+
+int main() {
+    CHECK(kSmemBytes + 4096 <= 232448, "shared memory %zu", (size_t)kSmemBytes);
+    // reduce buffers: rows of every W fit; every unit walk tiles its segment and each copy fits a row
+    for (int W = 1; W <= kMaxRanks; ++W) {
+        CHECK((int64_t)W * r_row(W) <= kRBufBytes, "rows W=%d", W);
+        CHECK(r_unit(W) >= 128 && r_unit(W) % 128 == 0 && r_unit(W) <= r_unit_max(W), "unit W=%d", W);
+        for (int trial = 0; trial < 4000; ++trial) {
+            const int64_t a = (int64_t)(next_u64() % 5000000);
+            const int64_t lens[] = {1, 2, 15, 16, 17, 127, 128, 129, r_unit(W) - 1, r_unit(W), r_unit(W) + 1,
+                                    r_unit_max(W), r_unit_max(W) + 1, 2 * r_unit(W) + 3, 4097, 4110,
+                                    (int64_t)(next_u64() % 400000) + 1};
+            const int64_t L = lens[trial % 17];
+            const int64_t b = a + L;
+            int64_t x = a;
+            int units = 0;
+            while (x < b) {
+                const int64_t c0 = unit_copy_start(x), xb = unit_end(x, b, W);
+                const int64_t nb = ((xb + 15) & ~(int64_t)15) - c0;
+                CHECK(c0 % 128 == 0 && c0 <= x && xb > x && xb <= b, "unit W=%d a=%lld L=%lld x=%lld", W,
+                      (long long)a, (long long)L, (long long)x);
+                CHECK(nb > 0 && nb % 16 == 0 && nb <= r_row(W), "copy W=%d nb=%lld row=%d", W, (long long)nb, r_row(W));
+                x = xb;
+                ++units;
+            }
+            CHECK(x == b && units <= (L + r_unit(W) - 1) / r_unit(W) + 1, "tiling W=%d L=%lld units=%d", W,
+                  (long long)L, units);
+        }
+    }
+    // gradient pieces: the last piece fits a slot, pieces tile the item, the pair's halves split each piece
+    for (int64_t bytes = 16; bytes <= (int64_t)40 * kPiece; bytes += 16) {
+        const int np = pieces_of(bytes);
+        CHECK(np >= 1 && (int64_t)(np - 1) * kPiece < bytes, "pieces %lld", (long long)bytes);
+        CHECK(bytes - (int64_t)(np - 1) * kPiece <= kSlotBytes, "last piece %lld", (long long)bytes);
+        const uint32_t ngroups = (uint32_t)(bytes / 16);
+        uint32_t covered = 0;
+        for (int p = 0; p < np; ++p) {
+            for (uint32_t half = 0; half < 2; ++half) {
+                const uint32_t gp = (uint32_t)p * kGroupsPerPiece + half * kHalfGroups;
+                const uint32_t ng = half_groups(p, np, half, gp, ngroups);
+                if (ng == 0) continue;
+                CHECK(gp == covered, "gap bytes=%lld p=%d half=%u", (long long)bytes, p, half);
+                CHECK((uint64_t)half * kHalfGroups * 16 + (uint64_t)ng * 16 <= (uint64_t)kSlotBytes,
+                      "half beyond its slot bytes=%lld p=%d", (long long)bytes, p);
+                covered = gp + ng;
+            }
+        }
+        CHECK(covered == ngroups, "groups bytes=%lld covered=%u of %u", (long long)bytes, covered, ngroups);
+    }
+    std::printf("ok\n");
+    return 0;
+}
+'''
+
+
+def test_pipe_geometry(tmp_path):
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not found")
+    src = tmp_path / "geom.cu"
+    src.write_text(PROGRAM)
+    exe = tmp_path / "geom"
+    subprocess.check_call([nvcc, "-std=c++17", "-O1", "-I" + CSRC, "-I" + os.path.join(ROOT, "include"),
+                           "-gencode", "arch=compute_103a,code=sm_103a", str(src), "-o", str(exe)])
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip() == "ok"
