@@ -13,14 +13,16 @@
 //     with it, so the copies of the next items are in flight while this one is quantised.  A chunk
 //     larger than the ring is copied twice (absmax pass, then quantise pass, the second from L2).
 //     The item then publishes one 64-bit word: this launch's tag and the scale bits, in one store.
-//   - Reduce items are (chunk j, segment t), t indexing torch.chunk(chunk, W) (the ring segments).
-//     Reducer warps wait (bounded) until the chunk's W words carry this launch's tag, read the
-//     segment's codes of every rank from L2 in the item's order, dequantise, sum, store the mean,
-//     and discard the code lines they alone read from L2 (discard.global.L2), so codes never travel
-//     to HBM.
-//   - Both kinds of item are claimed in chunk order from two 64-bit counters in the workspace, so
-//     every item is taken by a CTA that is running, quantise items never wait on reduce items, and
-//     every wait ends whatever the number of resident CTAs.
+//   - Reduce items are (chunk j, segment t), t indexing torch.chunk(chunk, W) (the ring segments; under
+//     the hierarchical order torch.chunk(chunk, L), the node segments).  A reduce producer warp waits
+//     (bounded) until the chunk's W words carry this launch's tag, then bulk-copies the segment's codes
+//     of every rank from L2 into a reduce buffer, a unit at a time; reducer warps dequantise, sum in the
+//     item's order, store the mean, and discard the code lines they alone read from L2
+//     (discard.global.L2), so codes never travel to HBM.  The kernel is built once per reducer kind
+//     (sequential and ring, tree, hierarchical), each with its own register allocation.
+//   - The first item of each kind of CTA b is item b; later ones are claimed in chunk order from two
+//     64-bit counters in the workspace.  Quantise items never wait on reduce items, so every wait ends
+//     as long as every CTA of the launch eventually starts.
 //
 // HBM sees the algorithmic traffic only: gradients read once, the mean written once.
 #pragma once
