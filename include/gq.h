@@ -255,7 +255,8 @@ size_t gq_pipelined_workspace_bytes(int W, size_t rank_stride, size_t num_chunks
  *     in time), the segment's codes are read back from L2, dequantised, summed in the order, averaged
  *     and stored, and their L2 lines dropped without a write-back.
  * HBM traffic is the gradients read once and the output written once.  Same arguments, results (bit
- * for bit) and errors as gq_fused_allreduce_sim, plus
+ * for bit) and errors as gq_fused_allreduce_sim, except that it also takes the hierarchical order
+ * (GQ_ORDER_HIER + L), plus
  *   d_found_inf_opt  NULL, or a device float set to 1.0f when an input value is Inf or NaN or
  *                    overflows when unscaled (as gq_fused_allreduce_sim_amp)
  *   d_workspace      device memory of at least gq_pipelined_workspace_bytes(W, rank_stride,
