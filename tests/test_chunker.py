@@ -2,6 +2,9 @@
 import numpy as np
 import pytest
 
+import __graft_entry__
+
+__graft_entry__.build()  # the package loads libgq.so on import (it has no fallback)
 from dp_gradient_bucket_gb300.chunker import DynamicChunker
 
 

@@ -10,6 +10,9 @@ import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
+import __graft_entry__
+
+__graft_entry__.build()  # the package loads libgq.so on import (it has no fallback)
 from dp_gradient_bucket_gb300 import shard
 
 
