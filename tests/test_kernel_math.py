@@ -168,3 +168,24 @@ def test_absmax_before_unscale():
         x = x[np.isfinite(x)]
         g = x * inv
         assert np.float32(np.abs(g).max()) == np.float32(np.abs(x).max() * inv)
+
+
+def test_packed_tie_filter_covers_the_scalar_filter():
+    """The pipelined kernel's packed filter sends a pair to the exact division when
+    fl(d * d - k) >= 0 (one fused rounding, k = 0.24993896484375, sign bit clear), d = t - rne(t).
+    Rounding never flips the sign of a nonzero result, so it flags exactly the d with d * d >= k.
+    Every binary32 d the scalar filter flags (|d| > 0.5 - 2^-14, up to |d| = 0.5) must be flagged:
+    all of them, by enumeration of the binary32 values in that band."""
+    k = np.float32(0.24993896484375)
+    assert np.array(k).view(np.uint32) == 0x3E7FF000
+    lo = np.array(NEAR_TIE, dtype=np.float32).view(np.uint32)
+    hi = np.array(np.float32(0.5), dtype=np.float32).view(np.uint32)
+    band = np.arange(lo + 1, hi + 1, dtype=np.uint32).view(np.float32)
+    assert band.size > 1000 and band.min() > NEAR_TIE and band.max() == 0.5
+    for d in (band, -band):
+        exact = d.astype(np.float64) ** 2 - np.float64(k)   # d*d is exact in binary64, as is the difference here
+        assert np.all(exact > 0)
+        assert np.all(np.float32(exact) >= 0)                # the fused result keeps the sign
+    # and it is not much wider: |d| below sqrt(k) by more than a few ulp is never flagged
+    below = np.float32(np.sqrt(np.float64(k))) - np.float32(2.0 ** -20)
+    assert np.float64(below) ** 2 - np.float64(k) < 0
