@@ -7,6 +7,9 @@ __frcp_rn / __fdiv_rn are), checked against the plain definition on many inputs.
    otherwise the kernel divides.
 2. The binary-counter pairwise tree pairs ranks exactly like the level-by-level rule.
 3. max|fl(x * inv)| == fl(max|x| * inv) (the absmax is taken before the unscale).
+4. The pipelined kernel's packed near-tie filter flags every quotient the scalar one flags.
+5. The reducers' code decode: a code byte XOR 0x80 placed as the low mantissa byte of 2^23 gives
+   2^23 + 128 + q, so subtracting 8388736 recovers q exactly; and fma(q, s, -0) rounds q * s once.
 """
 import numpy as np
 
@@ -189,3 +192,20 @@ def test_packed_tie_filter_covers_the_scalar_filter():
     # and it is not much wider: |d| below sqrt(k) by more than a few ulp is never flagged
     below = np.float32(np.sqrt(np.float64(k))) - np.float32(2.0 ** -20)
     assert np.float64(below) ** 2 - np.float64(k) < 0
+
+
+def test_code_byte_decode_and_product():
+    """Every int8 code: float(0x4B000000 | (byte ^ 0x80)) - 8388736 == q, exactly; and
+    fma(q, s, -0.0) == fl(q * s) for every code and a spread of scales (the product of two binary32
+    values is exact in binary64, adding -0 changes nothing, one rounding to binary32 follows)."""
+    q = np.arange(-128, 128, dtype=np.int64)
+    byte = (q & 0xFF).astype(np.uint32)
+    biased = (np.uint32(0x4B000000) | (byte ^ np.uint32(0x80))).view(np.float32)
+    assert np.array_equal((biased - np.float32(8388736.0)).astype(np.int64), q)
+    rng = np.random.default_rng(5)
+    s = (rng.random(2000) * 10.0 ** rng.uniform(-40, 36, 2000)).astype(np.float32)  # |q * s| stays finite
+    s = s[np.isfinite(s)]
+    qf = q.astype(np.float32)
+    prod = qf[:, None] * s[None, :]                                      # fl(q * s)
+    fused = (qf.astype(np.float64)[:, None] * s.astype(np.float64)[None, :] + (-0.0)).astype(np.float32)
+    assert np.array_equal(prod.view(np.uint32), fused.view(np.uint32))
